@@ -1,0 +1,8 @@
+"""GB300-native attention-prologue key path: fused KV RMSNorm + interleaved
+RoPE + quantise + cache scatter, and the QSA block-key prepare.
+
+The compute runs in hand-written sm_103a CUDA kernels behind the C ABI of
+libkvr.so (include/kvr.h); this package holds the thin ctypes binding, the
+build step and the seeded synthetic workloads. There is no CPU fallback:
+calling an entry point without the built library raises.
+"""

@@ -1,0 +1,30 @@
+"""Oracle: a plain, slow, obviously correct CPU (float64 NumPy) statement of
+what the attention-prologue key path computes.
+
+TEST INFRASTRUCTURE, NOT PRODUCT. Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import it. It shares no code with the CUDA
+path (no kernels, headers, helpers, tables or constants) and imports
+nothing from it; the only thing both sides use is the seeded input
+generator, which holds none of the method's arithmetic.
+
+Modules:
+  encoders               float64 -> cache codes (bf16, f16, int8, FP8 E4M3FN, FP8 E5M2)
+  kv_rmsnorm_rope_cache  RMSNorm + interleaved RoPE + quantise + scatter
+  qsa_prepare            QSA block-key prepare with carry across calls
+
+Every function is pinned by `-m "not gpu"` tests to closed forms, invariants,
+hand-worked toys (tests/golden) or library routines; no part is
+"parity unpinned".
+"""
+from . import encoders
+from .kv_rmsnorm_rope_cache import (NORM, PA_BLK_BSND, PA_BSND, STATUS_INDEX,
+                                    cache_slot, interleave_rope, quantise,
+                                    ref_kv_rmsnorm_rope_cache,
+                                    ref_kv_rmsnorm_rope_cache_loop, rms_norm)
+from .qsa_prepare import STATUS_BLOCK_CAP, STATUS_KEY_LENGTH, ref_qsa_prepare
+
+__all__ = [
+    "encoders", "NORM", "PA_BSND", "PA_BLK_BSND", "STATUS_INDEX", "STATUS_KEY_LENGTH",
+    "STATUS_BLOCK_CAP", "cache_slot", "interleave_rope", "quantise", "rms_norm",
+    "ref_kv_rmsnorm_rope_cache", "ref_kv_rmsnorm_rope_cache_loop", "ref_qsa_prepare",
+]

@@ -1,0 +1,93 @@
+"""Oracle for the QSA block-key prepare.
+
+Test infrastructure only (see oracle/__init__.py). Plain float64 NumPy,
+written from the page "openvino.opset17.qsa_prepare" (docs.openvino.ai):
+
+* summary: one index key per key block completed by the new tokens; a block
+  key is the mean of the raw index keys of the block's key_block_size
+  consecutive tokens, RMS-normalised with k_norm_weight, then rotated with
+  the RoPE of the block's first token; an empty input disables a feature.
+* parameters: raw_index_keys [N, L, Di]; past_block_index_keys [N, Bp, Di];
+  key_length [N] or [1] (valid key tokens per sequence); rope_cos/rope_sin
+  [N, L, Dr]; k_norm_weight [Di]; past_incomplete_raw_keys [N, kbs-1, Di];
+  past_incomplete_rope [N, 2*Dr] (cos and sin of the first token of the
+  incomplete block); key_block_size > 1; epsilon added to the mean square.
+
+Readings where the page is silent (each also listed with the design notes):
+* key_length counts the tokens after this call, so the past length is
+  P = key_length - L; a [1] key_length applies to every sequence.
+* Block keys live in a buffer indexed by absolute block number; block j
+  covers tokens [j*kbs, (j+1)*kbs); blocks before floor(P/kbs) and rows not
+  completed stay untouched.
+* The RMS normalisation is the one of the aclnnKvRmsNormRopeCache page
+  ("Formulas (2) rmsNorm"); an absent k_norm_weight disables the whole
+  normalisation.
+* The rotation is that page's interleaved RoPE ("Formulas (1)") on the last
+  Dr channels, with cos/sin of the block's first token: the new tables when
+  that token is new, else past_incomplete_rope laid out as [cos | sin].
+* Mean, normalisation and rotation are taken in float64 with one rounding to
+  bfloat16 at the end.
+* Carry-out (for chaining calls): the raw keys of the tokens after the last
+  completed block, and the cos/sin of the first of them.
+"""
+import numpy as np
+
+from . import encoders as enc
+from .kv_rmsnorm_rope_cache import interleave_rope, rms_norm
+
+STATUS_KEY_LENGTH = 0x2   # key_length[n] < L
+STATUS_BLOCK_CAP = 0x4    # a completed block's index is beyond the block-key buffer
+
+
+def ref_qsa_prepare(raw, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,
+                    past_raw, past_rope, key_block_size, eps=1e-6,
+                    next_raw=None, next_rope=None, out_dtype="bf16"):
+    """raw [N, L, Di] f64; block_keys codes [N, Bcap, Di] (written in place);
+    key_length int [N] or [1]; rope_cos/rope_sin [N, L, Dr] f64 or None;
+    k_norm_weight [Di] f64 or None; past_raw [N, kbs-1, Di] f64;
+    past_rope [N, 2*Dr] f64 or None; next_raw [N, kbs-1, Di] f64 / next_rope
+    [N, 2*Dr] f64 optional carry outputs (written in place).
+    Returns the device-status bits the call would raise."""
+    N, L, Di = raw.shape
+    kbs = int(key_block_size)
+    Bcap = block_keys.shape[1]
+    eps = float(np.float32(eps))
+    Dr = 0 if rope_cos is None else rope_cos.shape[-1]
+    status = 0
+    for n in range(N):
+        K = int(key_length[n if len(key_length) == N else 0])
+        P = K - L
+        if P < 0:
+            status |= STATUS_KEY_LENGTH
+            continue
+        f = P % kbs
+        F = P - f
+
+        def key(p):
+            return past_raw[n, p - F] if p < P else raw[n, p - P]
+
+        def rope_at(p):
+            if p >= P:
+                return rope_cos[n, p - P], rope_sin[n, p - P]
+            return past_rope[n, :Dr], past_rope[n, Dr:]
+
+        for j in range(P // kbs, K // kbs):
+            m = np.mean(np.stack([key(p) for p in range(j * kbs, (j + 1) * kbs)]), axis=0)
+            u = m if k_norm_weight is None else rms_norm(m, k_norm_weight, eps)
+            if rope_cos is not None:
+                c, s = rope_at(j * kbs)
+                u = np.concatenate((u[:Di - Dr], interleave_rope(u[Di - Dr:], c, s)))
+            if j >= Bcap:
+                status |= STATUS_BLOCK_CAP
+                continue
+            block_keys[n, j] = enc.encode(u, out_dtype)
+
+        Fn = (K // kbs) * kbs
+        if next_raw is not None:
+            for p in range(Fn, K):
+                next_raw[n, p - Fn] = key(p)
+        if next_rope is not None and rope_cos is not None and Fn < K:
+            c, s = rope_at(Fn)
+            next_rope[n, :Dr] = c
+            next_rope[n, Dr:] = s
+    return status

@@ -1,0 +1,155 @@
+"""Pins for the QSA block-key oracle: hand-worked toys (tests/golden), the
+no-norm/no-rope case against numpy's mean, chunking, constant keys, and the
+rule that unused carry rows are never read."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import encoders as enc
+from helpers import evs, golden, oracle_qsa_inputs, run_oracle_qsa
+from attention_prologue_kv_gb300 import workloads as wl
+
+
+def _golden_call(g, carry=False):
+    raw = np.array(g["raw"], dtype=np.float64)
+    N, L, Di = raw.shape
+    kbs = g["kbs"]
+    Dr = len(g["rope_cos"][0][0])
+    bk = np.full((N, g["Bcap"], Di), wl.SENTINEL16, dtype=np.uint16)
+    past_raw = np.array(g.get("past_raw", np.full((N, kbs - 1, Di), np.nan)), dtype=np.float64)
+    past_rope = np.array(g.get("past_rope", np.full((N, 2 * Dr), np.nan)), dtype=np.float64)
+    nr = np.full((N, kbs - 1, Di), np.nan) if carry else None
+    npr = np.full((N, 2 * Dr), np.nan) if carry else None
+    st = oracle.ref_qsa_prepare(raw, bk, np.array(g["key_length"]), np.array(g["rope_cos"], dtype=np.float64),
+                                np.array(g["rope_sin"], dtype=np.float64),
+                                np.array(g["k_norm_weight"], dtype=np.float64), past_raw, past_rope,
+                                kbs, g["eps"], next_raw=nr, next_rope=npr)
+    return bk, nr, npr, st
+
+
+@pytest.mark.parametrize("name", ["qsa_two_block.json", "qsa_carry.json"])
+def test_hand_worked_toys(name):
+    g = golden(name)
+    bk, nr, npr, st = _golden_call(g, carry=True)
+    assert st == 0
+    for j, exprs in g["expected_blocks"].items():
+        want = evs(exprs)
+        assert np.array_equal(bk[0, int(j)], enc.bf16_encode(want)), (j, enc.bf16_decode(bk[0, int(j)]), want)
+    for j in g["untouched_blocks"]:
+        assert np.all(bk[0, j] == wl.SENTINEL16)
+    if "expected_next_raw" in g:
+        rows = np.array(g["expected_next_raw"], dtype=object)
+        n_rows = rows.shape[1]
+        np.testing.assert_array_equal(nr[:, :n_rows], np.vectorize(float)(rows))
+        np.testing.assert_allclose(npr, np.vectorize(float)(np.array(g["expected_next_rope"], dtype=object)))
+
+
+def test_no_norm_no_rope_is_plain_block_mean():
+    case = wl.make_qsa_case("t", 3, 48, Di=24, kbs=8, seed=1, past=[0, 0, 0], rope=False, norm=False)
+    bk, _, _, st = run_oracle_qsa(case)
+    assert st == 0
+    raw = case.raw.to(torch.float64).numpy()
+    want = raw.reshape(3, 6, 8, 24).mean(axis=2)
+    assert np.array_equal(bk[:, :6], enc.bf16_encode(want))
+
+
+def test_constant_keys_mean_is_the_key_and_unit_weight_gives_unit_rms():
+    N, L, Di, kbs = 2, 16, 32, 4
+    raw = np.tile(np.random.default_rng(0).standard_normal((N, 1, Di)), (1, L, 1))
+    bk = np.full((N, 8, Di), wl.SENTINEL16, dtype=np.uint16)
+    oracle.ref_qsa_prepare(raw, bk, np.array([L, L]), None, None, None,
+                           np.full((N, kbs - 1, Di), np.nan), None, kbs)
+    for j in range(4):
+        assert np.array_equal(bk[:, j], enc.bf16_encode(raw[:, 0]))
+    eps = float(np.float32(1e-6))
+    bk2 = np.full((N, 8, Di), wl.SENTINEL16, dtype=np.uint16)
+    # capture the float64 result through a float64 "encoder": decode is exact for the bf16 output,
+    # so test the closed form on the float64 normalised vector directly
+    m = raw[:, 0]
+    u = oracle.rms_norm(m, np.ones(Di), eps)
+    ms = (m * m).mean(-1)
+    np.testing.assert_allclose(np.sqrt((u * u).mean(-1)), np.sqrt(ms / (ms + eps)), rtol=1e-13)
+    oracle.ref_qsa_prepare(raw, bk2, np.array([L]), None, None, np.ones(Di),
+                           np.full((N, kbs - 1, Di), np.nan), None, kbs)
+    assert np.array_equal(bk2[:, 0], enc.bf16_encode(u))
+
+
+def test_chunked_calls_equal_one_call():
+    """One call over L tokens equals three chained calls over pieces of L,
+    each feeding the next through the carry outputs."""
+    N, L, Di, Dr, kbs = 4, 45, 16, 8, 6
+    case = wl.make_qsa_case("t", N, L, Di=Di, Dr=Dr, kbs=kbs, seed=3, past=[0, 5, 13, 6], Bcap=12)
+    whole, _, _, st = run_oracle_qsa(case)
+    assert st == 0
+    inp = oracle_qsa_inputs(case)
+    P = np.array(case.meta["past"])
+    pieces = [0, 7, 30, L]
+    bk = np.full_like(whole, wl.SENTINEL16)
+    past_raw, past_rope = inp["past_raw"], inp["past_rope"]
+    for a, b in zip(pieces[:-1], pieces[1:]):
+        nr = np.full((N, kbs - 1, Di), np.nan)
+        npr = np.full((N, 2 * Dr), np.nan)
+        st = oracle.ref_qsa_prepare(inp["raw"][:, a:b], bk, P + b, inp["rope_cos"][:, a:b],
+                                    inp["rope_sin"][:, a:b], inp["k_norm_weight"], past_raw,
+                                    past_rope, kbs, case.eps, next_raw=nr, next_rope=npr)
+        assert st == 0
+        # an unspecified carry rope (no incomplete block) stays NaN: it must never be read
+        past_raw, past_rope = nr, npr
+    assert np.array_equal(bk, whole)
+
+
+def test_unused_carry_rows_are_never_read():
+    case = wl.qsa_prepare_workload()
+    bk, _, _, st = run_oracle_qsa(case)
+    assert st == 0
+    vals = enc.bf16_decode(bk[bk != wl.SENTINEL16])
+    assert np.all(np.isfinite(vals))
+    # 32 completed blocks per sequence (L = 2048 = 32 * 64)
+    written = (bk != wl.SENTINEL16).all(-1)
+    assert written.sum() == 32 * 32
+    P = np.array(case.meta["past"])
+    for n in range(case.N):
+        assert np.array_equal(np.nonzero(written[n])[0], np.arange(P[n] // 64, P[n] // 64 + 32))
+
+
+def test_shared_key_length_broadcasts():
+    case = wl.make_qsa_case("t", 3, 20, Di=16, Dr=8, kbs=4, seed=5, shared_length=True)
+    bk1, _, _, st = run_oracle_qsa(case)
+    case.key_length = case.key_length.expand(3).clone()
+    bk2, _, _, _ = run_oracle_qsa(case)
+    assert st == 0 and np.array_equal(bk1, bk2)
+
+
+def test_short_key_length_and_block_cap_raise_status():
+    case = wl.make_qsa_case("t", 2, 16, Di=16, Dr=8, kbs=4, seed=6, past=[0, 3])
+    case.key_length = torch.tensor([10, 19])   # sequence 0: key_length < L
+    bk, _, _, st = run_oracle_qsa(case)
+    assert st == oracle.STATUS_KEY_LENGTH
+    assert np.all(bk[0] == wl.SENTINEL16)
+    case = wl.make_qsa_case("t", 1, 16, Di=16, Dr=8, kbs=4, seed=6, past=[0], Bcap=2)
+    bk, _, _, st = run_oracle_qsa(case)
+    assert st == oracle.STATUS_BLOCK_CAP
+    assert (bk[0] != wl.SENTINEL16).all(-1).sum() == 2
+
+
+def test_rope_uses_first_token_of_block_on_last_dr_channels():
+    """Rotating the tables of a block's non-first tokens changes nothing;
+    rotating the first token's changes only the last Dr channels."""
+    case = wl.make_qsa_case("t", 2, 32, Di=16, Dr=8, kbs=4, seed=8, past=[0, 2])
+    bk, _, _, _ = run_oracle_qsa(case)
+    c2 = wl.make_qsa_case("t", 2, 32, Di=16, Dr=8, kbs=4, seed=8, past=[0, 2])
+    P = np.array([0, 2])
+    for n in range(2):
+        for t in range(32):
+            if (P[n] + t) % 4 != 0:
+                c2.rope_cos[n, t] = 7.0
+                c2.rope_sin[n, t] = -3.0
+    bk2, _, _, _ = run_oracle_qsa(c2)
+    assert np.array_equal(bk, bk2)
+    c3 = wl.make_qsa_case("t", 2, 32, Di=16, Dr=8, kbs=4, seed=8, past=[0, 2])
+    c3.rope_cos[0, 4] = 0.0
+    c3.rope_sin[0, 4] = 1.0
+    bk3, _, _, _ = run_oracle_qsa(c3)
+    assert np.array_equal(bk3[0, 1, :8], bk[0, 1, :8])
+    assert not np.array_equal(bk3[0, 1, 8:], bk[0, 1, 8:])
