@@ -1,0 +1,194 @@
+"""Python entry points: marshal torch CUDA tensors into the C ABI of
+libkvr.so and call it on the current (or given) stream. Argument checking
+beyond marshalling (shapes, ranges, aliasing) is done by the library, whose
+status is raised as KvrError. Calls are asynchronous; nothing synchronises."""
+import ctypes
+
+import torch
+
+from . import _native as N
+
+_IN_DTYPES = {torch.bfloat16: N.KVR_BF16, torch.float16: N.KVR_F16}
+_CACHE_DTYPES = {
+    torch.bfloat16: N.KVR_BF16,
+    torch.float16: N.KVR_F16,
+    torch.int8: N.KVR_INT8,
+    torch.float8_e4m3fn: N.KVR_FP8_E4M3FN,
+    torch.float8_e5m2: N.KVR_FP8_E5M2,
+}
+
+
+class KvrError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = int(code)
+        super().__init__("%s: %s (status %d)" % (where, N.status_string(code), self.code))
+
+
+def _cuda(t, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor: the kernels run on the GPU only" % name)
+    return t
+
+
+def _ptr(t, name, contiguous=True):
+    if t is None:
+        return None
+    _cuda(t, name)
+    if contiguous and not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _kv_rows(kv):
+    """(Bkv, Skv, row stride in elements) of a [Bkv,1,Skv,D] / [Bkv,Skv,D] / [T,D]
+    tensor whose rows are uniformly strided and whose last dim is dense."""
+    if kv.stride(-1) != 1:
+        raise ValueError("kv must be dense along its last dimension")
+    if kv.dim() == 4:
+        if kv.shape[1] != 1:
+            raise ValueError("kv must be [Bkv, 1, Skv, D]: the head axis N is 1")
+        B, S = kv.shape[0], kv.shape[2]
+        sb, ss = kv.stride(0), kv.stride(2)
+    elif kv.dim() == 3:
+        B, S = kv.shape[0], kv.shape[1]
+        sb, ss = kv.stride(0), kv.stride(1)
+    elif kv.dim() == 2:
+        B, S = kv.shape[0], 1
+        sb, ss = kv.stride(0), kv.stride(0)
+    else:
+        raise ValueError("kv must be 2-D, 3-D or 4-D")
+    stride = ss if S > 1 else sb
+    if B > 1 and S > 0 and sb != S * stride:
+        raise ValueError("kv rows must be uniformly strided")
+    return B, S, stride
+
+
+def _cache_dims(c, name):
+    _cuda(c, name)
+    if not c.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if c.dim() == 4 and c.shape[2] != 1:
+        raise ValueError("%s must be [d0, d1, 1, D*]" % name)
+    if c.dim() not in (3, 4):
+        raise ValueError("%s must be [d0, d1, 1, D*] or [d0, d1, D*]" % name)
+    if c.dtype not in _CACHE_DTYPES:
+        raise ValueError("%s has unsupported dtype %s" % (name, c.dtype))
+    return c.shape[0], c.shape[1], c.shape[-1]
+
+
+def kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
+                          cache_mode="PA_BSND", eps=1e-6, ckv_scale=None, k_scale=None,
+                          kc_scale=1.0, dev_status=None, stream=None):
+    """Fused RMSNorm(kv[..., :Dv]) -> ckv_cache and interleaved RoPE(kv[..., Dv:]) ->
+    k_cache, scattered by `index` (-1 skips). Dv = gamma.numel().
+
+    kv [Bkv, 1, Skv, D] (bf16/f16; rows may be strided, e.g. a column slice),
+    cos/sin [Bkv, 1, Skv, Dk], index int64 (layout per cache_mode),
+    caches [d0, d1, 1, Dv] and [d0, d1, 1, Dk] (bf16/f16 like kv, or int8 /
+    float8_e4m3fn / float8_e5m2 with a float32 scale of length D* or 1).
+    `dev_status` (int32, 1 element) collects device-side error bits."""
+    _cuda(kv, "kv")
+    Bkv, Skv, stride = _kv_rows(kv)
+    if kv.dtype not in _IN_DTYPES:
+        raise ValueError("kv must be bfloat16 or float16")
+    Dv = gamma.numel()
+    Dk = kv.shape[-1] - Dv
+    d0, d1, _ = _cache_dims(ckv_cache, "ckv_cache")
+    k0, k1, _ = _cache_dims(k_cache, "k_cache")
+    if (k0, k1) != (d0, d1):
+        raise ValueError("ckv_cache and k_cache must share their leading dims")
+    if cache_mode not in N.CACHE_MODES:
+        raise ValueError("cache_mode must be one of %s" % list(N.CACHE_MODES))
+    for t, name in ((gamma, "gamma"), (cos, "cos"), (sin, "sin")):
+        if t.dtype != kv.dtype:
+            raise ValueError("%s must have kv's dtype" % name)
+    if index.dtype != torch.int64:
+        raise ValueError("index must be int64")
+    for t, name in ((ckv_scale, "ckv_scale"), (k_scale, "k_scale")):
+        if t is not None and t.dtype != torch.float32:
+            raise ValueError("%s must be float32" % name)
+    if dev_status is not None and dev_status.dtype != torch.int32:
+        raise ValueError("dev_status must be int32")
+    a = N.KvArgs(
+        kv=kv.data_ptr(), in_dtype=_IN_DTYPES[kv.dtype], Bkv=Bkv, Skv=Skv, Dv=Dv, Dk=Dk,
+        kv_row_stride=stride, gamma=_ptr(gamma, "gamma"), cos=_ptr(cos, "cos"),
+        sin=_ptr(sin, "sin"), index=_ptr(index, "index"), mode=N.CACHE_MODES[cache_mode],
+        cache_d0=d0, cache_d1=d1,
+        ckv_cache=ckv_cache.data_ptr(), ckv_dtype=_CACHE_DTYPES[ckv_cache.dtype],
+        ckv_scale=_ptr(ckv_scale, "ckv_scale"),
+        ckv_scale_len=0 if ckv_scale is None else ckv_scale.numel(),
+        k_cache=k_cache.data_ptr(), k_dtype=_CACHE_DTYPES[k_cache.dtype],
+        k_scale=_ptr(k_scale, "k_scale"), k_scale_len=0 if k_scale is None else k_scale.numel(),
+        eps=float(eps), kc_scale=float(kc_scale), dev_status=_ptr(dev_status, "dev_status"))
+    st = N.lib().kv_rmsnorm_rope_cache(ctypes.byref(a), _stream(stream))
+    if st != N.KVR_OK:
+        raise KvrError(st, "kv_rmsnorm_rope_cache")
+
+
+def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,
+                past_incomplete_raw_keys, past_incomplete_rope, key_block_size, epsilon=1e-6, *,
+                next_incomplete_raw_keys=None, next_incomplete_rope=None, dev_status=None,
+                stream=None):
+    """QSA block-key prepare. Positional arguments follow the qsa_prepare
+    parameter list; `block_keys` [N, Bcap, Di] holds the past block keys and
+    receives the new ones in place (block j at row j). rope_cos/rope_sin
+    [N, L, Dr] (or both None), k_norm_weight [Di] or None,
+    past_incomplete_raw_keys [N, kbs-1, Di], past_incomplete_rope [N, 2*Dr] or
+    None, key_length int64 [N] or [1] = valid tokens after this call.
+    Optional carry outputs next_incomplete_raw_keys / next_incomplete_rope."""
+    raw = _cuda(raw_index_keys, "raw_index_keys")
+    if raw.dim() != 3:
+        raise ValueError("raw_index_keys must be [N, L, Di]")
+    if raw.dtype not in _IN_DTYPES:
+        raise ValueError("raw_index_keys must be bfloat16 or float16")
+    Nn, L, Di = raw.shape
+    if block_keys.dim() != 3 or block_keys.dtype != raw.dtype:
+        raise ValueError("block_keys must be [N, Bcap, Di] with raw_index_keys' dtype")
+    if key_length.dtype != torch.int64:
+        raise ValueError("key_length must be int64")
+    for t, name in ((rope_cos, "rope_cos"), (rope_sin, "rope_sin"), (k_norm_weight, "k_norm_weight"),
+                    (past_incomplete_raw_keys, "past_incomplete_raw_keys"),
+                    (past_incomplete_rope, "past_incomplete_rope"),
+                    (next_incomplete_raw_keys, "next_incomplete_raw_keys"),
+                    (next_incomplete_rope, "next_incomplete_rope")):
+        if t is not None and t.dtype != raw.dtype:
+            raise ValueError("%s must have raw_index_keys' dtype" % name)
+    if dev_status is not None and dev_status.dtype != torch.int32:
+        raise ValueError("dev_status must be int32")
+    Dr = rope_cos.shape[-1] if rope_cos is not None else 0
+    a = N.QsaArgs(
+        raw_index_keys=_ptr(raw, "raw_index_keys"), in_dtype=_IN_DTYPES[raw.dtype], N=Nn, L=L, Di=Di,
+        block_keys=_ptr(block_keys, "block_keys"), Bcap=block_keys.shape[1],
+        key_length=_ptr(key_length, "key_length"), key_length_len=key_length.numel(),
+        rope_cos=_ptr(rope_cos, "rope_cos"), rope_sin=_ptr(rope_sin, "rope_sin"), Dr=Dr,
+        k_norm_weight=_ptr(k_norm_weight, "k_norm_weight"),
+        past_incomplete_raw_keys=_ptr(past_incomplete_raw_keys, "past_incomplete_raw_keys"),
+        past_incomplete_rope=_ptr(past_incomplete_rope, "past_incomplete_rope"),
+        key_block_size=int(key_block_size), eps=float(epsilon),
+        next_incomplete_raw_keys=_ptr(next_incomplete_raw_keys, "next_incomplete_raw_keys"),
+        next_incomplete_rope=_ptr(next_incomplete_rope, "next_incomplete_rope"),
+        dev_status=_ptr(dev_status, "dev_status"))
+    if block_keys.shape[0] != Nn or block_keys.shape[2] != Di:
+        raise ValueError("block_keys must be [N, Bcap, Di]")
+    st = N.lib().qsa_prepare(ctypes.byref(a), _stream(stream))
+    if st != N.KVR_OK:
+        raise KvrError(st, "qsa_prepare")
+
+
+def device_copy(dst, src, stream=None):
+    """16-byte vectorised device copy of src into dst (same byte size); the
+    in-process HBM bandwidth reference."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src must have the same byte size")
+    st = N.lib().kvr_device_copy(_ptr(dst, "dst"), _ptr(src, "src"), nbytes, _stream(stream))
+    if st != N.KVR_OK:
+        raise KvrError(st, "kvr_device_copy")

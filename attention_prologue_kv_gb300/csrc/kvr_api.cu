@@ -1,0 +1,254 @@
+// Host side of libkvr.so: argument validation, kernel selection, launch.
+// Every entry point returns before launching anything when its arguments
+// are invalid; see include/kvr.h for the contract.
+#include <mutex>
+
+#include "kvr_internal.cuh"
+
+namespace kvr {
+
+int sm_count_current_device() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = 1;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// 16-byte vectorised copy for the in-process bandwidth reference.
+__global__ void __launch_bounds__(256) device_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                          int64_t n) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = ld_stream_v4(src + i);
+}
+
+cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s) {
+    const int64_t n = bytes / 16;
+    const int64_t cap = int64_t(sm_count_current_device()) * 8;
+    int64_t grid = (n + 255) / 256;
+    if (grid > cap) grid = cap;
+    device_copy_kernel<<<int(grid), 256, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), n);
+    return cudaGetLastError();
+}
+
+}  // namespace kvr
+
+using namespace kvr;
+
+namespace {
+
+bool is16(kvr_dtype d) { return d == KVR_BF16 || d == KVR_F16; }
+bool is8(kvr_dtype d) { return d == KVR_INT8 || d == KVR_FP8_E4M3FN || d == KVR_FP8_E5M2; }
+
+int out_kind(kvr_dtype d) {
+    switch (d) {
+        case KVR_INT8: return OUT_I8;
+        case KVR_FP8_E4M3FN: return OUT_E4M3;
+        case KVR_FP8_E5M2: return OUT_E5M2;
+        default: return OUT16;
+    }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Do the byte ranges [a, a+na) and [b, b+nb) overlap?
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+    if (a == nullptr || b == nullptr || na <= 0 || nb <= 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + uintptr_t(nb) && y < x + uintptr_t(na);
+}
+
+kvr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVR_OK : KVR_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int kvr_abi_version(void) { return KVR_ABI_VERSION; }
+
+const char* kvr_status_string(kvr_status s) {
+    switch (s) {
+        case KVR_OK: return "ok";
+        case KVR_ERR_NULL: return "a required pointer is NULL, or an optional pair is half given";
+        case KVR_ERR_SHAPE: return "a size is outside its documented range";
+        case KVR_ERR_DTYPE: return "an element type is not supported for that argument";
+        case KVR_ERR_MODE: return "unknown cache mode";
+        case KVR_ERR_ALIAS: return "an output overlaps an input it must not overlap";
+        case KVR_ERR_CUDA: return "the CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
+    if (a == nullptr) return KVR_ERR_NULL;
+    if (a->Bkv < 0 || a->Skv < 0 || a->Dv < 1 || a->Dk < 2 || (a->Dk & 1) || a->cache_d0 < 1 ||
+        a->cache_d1 < 1 || a->Dv > (int64_t(1) << 30) || a->Dk > (int64_t(1) << 30))
+        return KVR_ERR_SHAPE;
+    if (a->mode != KVR_CACHE_NORM && a->mode != KVR_CACHE_PA_BSND && a->mode != KVR_CACHE_PA_BLK_BSND)
+        return KVR_ERR_MODE;
+    if (!is16(a->in_dtype)) return KVR_ERR_DTYPE;
+    if (!(a->ckv_dtype == a->in_dtype || is8(a->ckv_dtype))) return KVR_ERR_DTYPE;
+    if (!(a->k_dtype == a->in_dtype || is8(a->k_dtype))) return KVR_ERR_DTYPE;
+    const int64_t D = a->Dv + a->Dk;
+    const int64_t stride = a->kv_row_stride == 0 ? D : a->kv_row_stride;
+    if (stride < D) return KVR_ERR_SHAPE;
+    if (a->mode == KVR_CACHE_NORM && a->cache_d0 < a->Bkv) return KVR_ERR_SHAPE;
+    if (!(a->eps >= 0.f) || !(a->kc_scale == a->kc_scale)) return KVR_ERR_SHAPE;
+    const int64_t T = a->Bkv * a->Skv;
+    if (T == 0) return KVR_OK;   // empty input: caches are not updated
+    if (a->kv == nullptr || a->gamma == nullptr || a->cos == nullptr || a->sin == nullptr ||
+        a->index == nullptr || a->ckv_cache == nullptr || a->k_cache == nullptr)
+        return KVR_ERR_NULL;
+    // 8-bit caches need their scale, 16-bit caches take none.
+    if (is8(a->ckv_dtype) != (a->ckv_scale != nullptr)) return KVR_ERR_NULL;
+    if (is8(a->k_dtype) != (a->k_scale != nullptr)) return KVR_ERR_NULL;
+    if (a->ckv_scale != nullptr && a->ckv_scale_len != a->Dv && a->ckv_scale_len != 1) return KVR_ERR_SHAPE;
+    if (a->k_scale != nullptr && a->k_scale_len != a->Dk && a->k_scale_len != 1) return KVR_ERR_SHAPE;
+    if (!aligned(a->kv, 2) || !aligned(a->gamma, 2) || !aligned(a->cos, 2) || !aligned(a->sin, 2) ||
+        !aligned(a->index, 8) || !aligned(a->ckv_scale, 4) || !aligned(a->k_scale, 4) ||
+        (is16(a->ckv_dtype) && !aligned(a->ckv_cache, 2)) || (is16(a->k_dtype) && !aligned(a->k_cache, 2)))
+        return KVR_ERR_SHAPE;
+
+    const int64_t nblk = (a->Skv + a->cache_d1 - 1) / a->cache_d1;
+    const int64_t n_index = a->mode == KVR_CACHE_PA_BLK_BSND ? a->Bkv * nblk : T;
+    const int64_t rows = a->cache_d0 * a->cache_d1;
+    const int64_t ckv_bytes = rows * a->Dv * (is16(a->ckv_dtype) ? 2 : 1);
+    const int64_t k_bytes = rows * a->Dk * (is16(a->k_dtype) ? 2 : 1);
+    const int64_t kv_bytes = ((T - 1) * stride + D) * 2;
+    const void* ins[] = {a->kv, a->gamma, a->cos, a->sin, a->index, a->ckv_scale, a->k_scale};
+    const int64_t in_bytes[] = {kv_bytes, a->Dv * 2, T * a->Dk * 2, T * a->Dk * 2, n_index * 8,
+                                a->ckv_scale_len * 4, a->k_scale_len * 4};
+    for (int i = 0; i < 7; ++i)
+        if (overlap(a->ckv_cache, ckv_bytes, ins[i], in_bytes[i]) || overlap(a->k_cache, k_bytes, ins[i], in_bytes[i]))
+            return KVR_ERR_ALIAS;
+    if (overlap(a->ckv_cache, ckv_bytes, a->k_cache, k_bytes)) return KVR_ERR_ALIAS;
+
+    KvParams p;
+    p.kv = a->kv;
+    p.gamma = a->gamma;
+    p.cos = a->cos;
+    p.sin = a->sin;
+    p.index = a->index;
+    p.ckv = a->ckv_cache;
+    p.kc = a->k_cache;
+    p.ckv_scale = a->ckv_scale;
+    p.k_scale = a->k_scale;
+    p.status = a->dev_status;
+    p.T = T;
+    p.Skv = a->Skv;
+    p.kv_stride = stride;
+    p.d0 = a->cache_d0;
+    p.d1 = a->cache_d1;
+    p.nblk = nblk;
+    p.Dv = int(a->Dv);
+    p.Dk = int(a->Dk);
+    p.mode = int(a->mode);
+    p.k_kind = out_kind(a->k_dtype);
+    p.ckv_scale_per_ch = a->ckv_scale_len == a->Dv && a->Dv > 1;
+    p.k_scale_per_ch = a->k_scale_len == a->Dk;
+    p.eps = a->eps;
+    p.inv_dv = 1.0f / float(a->Dv);
+    p.alpha = a->kc_scale;
+
+    const bool ckv8 = is8(a->ckv_dtype), k8 = is8(a->k_dtype);
+    const bool vec = (a->Dv % 8 == 0) && a->Dv <= 1024 && (a->Dk % 8 == 0) && a->Dk <= 256 && (stride % 8 == 0) &&
+                     aligned(a->kv, 16) && aligned(a->gamma, 16) && aligned(a->cos, 16) && aligned(a->sin, 16) &&
+                     aligned(a->ckv_cache, ckv8 ? 8 : 16) && aligned(a->k_cache, k8 ? 4 : 8);
+    (void)cudaGetLastError();
+    return cuda_status(launch_kv(p, a->in_dtype, out_kind(a->ckv_dtype), vec, stream));
+}
+
+kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
+    if (a == nullptr) return KVR_ERR_NULL;
+    if (!is16(a->in_dtype)) return KVR_ERR_DTYPE;
+    const bool rope = a->rope_cos != nullptr || a->rope_sin != nullptr;
+    if (a->N < 0 || a->L < 0 || a->Di < 1 || a->Di > 4096 || a->Bcap < 1 || a->key_block_size < 2 ||
+        (a->key_length_len != 1 && a->key_length_len != a->N))
+        return KVR_ERR_SHAPE;
+    if (rope && (a->Dr < 2 || (a->Dr & 1) || a->Dr > a->Di)) return KVR_ERR_SHAPE;
+    if (!(a->eps >= 0.f)) return KVR_ERR_SHAPE;
+    if (a->N * a->L == 0) return KVR_OK;
+    if (a->raw_index_keys == nullptr || a->block_keys == nullptr || a->key_length == nullptr ||
+        a->past_incomplete_raw_keys == nullptr)
+        return KVR_ERR_NULL;
+    if (rope && (a->rope_cos == nullptr || a->rope_sin == nullptr || a->past_incomplete_rope == nullptr))
+        return KVR_ERR_NULL;
+    if (!rope && a->past_incomplete_rope != nullptr) return KVR_ERR_NULL;
+    if (!rope && a->next_incomplete_rope != nullptr) return KVR_ERR_NULL;
+    const int64_t nbmax = (a->L + a->key_block_size - 1) / a->key_block_size;
+    if (a->N * (nbmax + 1) > 0x7FFFFFFFLL) return KVR_ERR_SHAPE;
+    const void* ptrs[] = {a->raw_index_keys, a->block_keys, a->rope_cos, a->rope_sin, a->k_norm_weight,
+                          a->past_incomplete_raw_keys, a->past_incomplete_rope, a->next_incomplete_raw_keys,
+                          a->next_incomplete_rope};
+    for (const void* q : ptrs)
+        if (!aligned(q, 2)) return KVR_ERR_SHAPE;
+    if (!aligned(a->key_length, 8)) return KVR_ERR_SHAPE;
+
+    const int64_t Dr = rope ? a->Dr : 0;
+    const int64_t kbs = a->key_block_size;
+    const int64_t nr_bytes = a->N * (kbs - 1) * a->Di * 2;
+    const int64_t nrope_bytes = a->N * 2 * Dr * 2;
+    const void* ins[] = {a->raw_index_keys, a->block_keys, a->rope_cos, a->rope_sin, a->k_norm_weight,
+                         a->past_incomplete_raw_keys, a->past_incomplete_rope, a->key_length};
+    const int64_t in_bytes[] = {a->N * a->L * a->Di * 2, a->N * a->Bcap * a->Di * 2, a->N * a->L * Dr * 2,
+                                a->N * a->L * Dr * 2, a->Di * 2, nr_bytes, nrope_bytes, a->key_length_len * 8};
+    for (int i = 0; i < 8; ++i)
+        if (overlap(a->next_incomplete_raw_keys, nr_bytes, ins[i], in_bytes[i]) ||
+            overlap(a->next_incomplete_rope, nrope_bytes, ins[i], in_bytes[i]))
+            return KVR_ERR_ALIAS;
+    if (overlap(a->next_incomplete_raw_keys, nr_bytes, a->next_incomplete_rope, nrope_bytes)) return KVR_ERR_ALIAS;
+    for (int i = 0; i < 8; ++i)
+        if (i != 1 && overlap(a->block_keys, in_bytes[1], ins[i], in_bytes[i])) return KVR_ERR_ALIAS;
+
+    QsaParams p;
+    p.raw = a->raw_index_keys;
+    p.block_keys = a->block_keys;
+    p.key_length = a->key_length;
+    p.cos = a->rope_cos;
+    p.sin = a->rope_sin;
+    p.w = a->k_norm_weight;
+    p.past_raw = a->past_incomplete_raw_keys;
+    p.past_rope = a->past_incomplete_rope;
+    p.next_raw = a->next_incomplete_raw_keys;
+    p.next_rope = a->next_incomplete_rope;
+    p.status = a->dev_status;
+    p.N = a->N;
+    p.L = a->L;
+    p.Bcap = a->Bcap;
+    p.kbs = kbs;
+    p.nbmax = nbmax;
+    p.key_length_per_seq = a->key_length_len == a->N && a->N > 1;
+    p.Di = int(a->Di);
+    p.Dr = int(Dr);
+    p.eps = a->eps;
+    p.inv_di = 1.0f / float(a->Di);
+    p.inv_kbs = 1.0f / float(kbs);
+
+    const bool vec = (a->Di % 8 == 0) && aligned(a->raw_index_keys, 16) && aligned(a->past_incomplete_raw_keys, 16);
+    (void)cudaGetLastError();
+    return cuda_status(launch_qsa(p, a->in_dtype, vec, stream));
+}
+
+kvr_status kvr_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream) {
+    if (bytes == 0) return KVR_OK;
+    if (dst == nullptr || src == nullptr) return KVR_ERR_NULL;
+    if (bytes < 0 || bytes % 16 != 0 || !aligned(dst, 16) || !aligned(src, 16)) return KVR_ERR_SHAPE;
+    if (overlap(dst, bytes, src, bytes)) return KVR_ERR_ALIAS;
+    (void)cudaGetLastError();
+    return cuda_status(launch_device_copy(dst, src, bytes, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+// Internal declarations and device helpers shared by the libkvr.so kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvr.h"
+
+namespace kvr {
+
+// ---------------------------------------------------------------------------
+// Element types
+// ---------------------------------------------------------------------------
+
+// Output element kinds. OUT16 is the 16-bit input type itself (bf16 or f16).
+enum OutKind : int { OUT16 = 0, OUT_I8 = 1, OUT_E4M3 = 2, OUT_E5M2 = 3 };
+
+struct BF16 {
+    static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
+    static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+    static __device__ __forceinline__ float one(uint16_t u) { return __uint_as_float(uint32_t(u) << 16); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ uint16_t one_out(float v) {
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        return *reinterpret_cast<uint16_t*>(&h);
+    }
+};
+
+struct F16 {
+    static __device__ __forceinline__ float lo(uint32_t u) { return __half2float(__ushort_as_half(uint16_t(u & 0xFFFFu))); }
+    static __device__ __forceinline__ float hi(uint32_t u) { return __half2float(__ushort_as_half(uint16_t(u >> 16))); }
+    static __device__ __forceinline__ float one(uint16_t u) { return __half2float(__ushort_as_half(u)); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ uint16_t one_out(float v) { return __half_as_ushort(__float2half_rn(v)); }
+};
+
+// Two floats -> two 8-bit codes packed in 16 bits (lo in the low byte).
+template <int K>
+__device__ __forceinline__ uint32_t enc8x2(float lo, float hi) {
+    if constexpr (K == OUT_E4M3) {
+        uint16_t r;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+        return r;
+    } else if constexpr (K == OUT_E5M2) {
+        uint16_t r;
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+        return r;
+    } else {  // OUT_I8: round half to even, clamp to [-128, 127]
+        int a = min(max(__float2int_rn(lo), -128), 127);
+        int b = min(max(__float2int_rn(hi), -128), 127);
+        return (uint32_t(a) & 0xFFu) | ((uint32_t(b) & 0xFFu) << 8);
+    }
+}
+
+// Runtime-kind variant for the small k-cache part.
+__device__ __forceinline__ uint32_t enc8x2_rt(int kind, float lo, float hi) {
+    if (kind == OUT_E4M3) return enc8x2<OUT_E4M3>(lo, hi);
+    if (kind == OUT_E5M2) return enc8x2<OUT_E5M2>(lo, hi);
+    return enc8x2<OUT_I8>(lo, hi);
+}
+
+// ---------------------------------------------------------------------------
+// Memory helpers
+// ---------------------------------------------------------------------------
+
+// Streaming read-only loads: inputs are read once, keep them out of L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ int64_t ld_stream_s64(const int64_t* p) {
+    int64_t r;
+    asm("ld.global.nc.L1::no_allocate.s64 %0, [%1];" : "=l"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Parameter blocks (passed by value to the kernels)
+// ---------------------------------------------------------------------------
+
+struct KvParams {
+    const void* kv;
+    const void* gamma;
+    const void* cos;
+    const void* sin;
+    const int64_t* index;
+    void* ckv;
+    void* kc;
+    const float* ckv_scale;
+    const float* k_scale;
+    int32_t* status;
+    int64_t T;           // token rows
+    int64_t Skv;
+    int64_t kv_stride;   // elements between consecutive kv rows
+    int64_t d0, d1;      // cache leading dims
+    int64_t nblk;        // PA_BLK_BSND: index entries per sequence
+    int Dv, Dk;
+    int mode;            // kvr_cache_mode
+    int k_kind;          // OutKind of the k cache
+    int ckv_scale_per_ch, k_scale_per_ch;
+    float eps, inv_dv, alpha;
+};
+
+struct QsaParams {
+    const void* raw;
+    void* block_keys;
+    const int64_t* key_length;
+    const void* cos;
+    const void* sin;
+    const void* w;
+    const void* past_raw;
+    const void* past_rope;
+    void* next_raw;
+    void* next_rope;
+    int32_t* status;
+    int64_t N, L, Bcap, kbs;
+    int64_t nbmax;       // CTAs per sequence for block keys = ceil(L / kbs)
+    int key_length_per_seq;
+    int Di, Dr;
+    float eps, inv_di, inv_kbs;
+};
+
+// Launchers (host), defined next to their kernels. Return a CUDA error code.
+cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, bool vec, cudaStream_t s);
+cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, cudaStream_t s);
+cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s);
+
+int sm_count_current_device();
+
+}  // namespace kvr

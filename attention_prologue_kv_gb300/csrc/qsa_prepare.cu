@@ -1,0 +1,203 @@
+// QSA block-key prepare: one key per key block completed by the new tokens.
+//
+// Operation: "openvino.opset17.qsa_prepare" (docs.openvino.ai), summary and
+// Parameters: block key = mean of the block's key_block_size raw index keys,
+// RMS-normalised with k_norm_weight, rotated with the RoPE of the block's
+// first token; past tokens of the incomplete block come from the carried
+// past_incomplete_raw_keys / past_incomplete_rope. The normalisation and the
+// rotation are the rmsNorm / interleaveRope formulas of
+// "aclnnKvRmsNormRopeCache" ("Formulas (1)", "Formulas (2)"), the rotation on
+// the last Dr channels.
+//
+// Design: one CTA per (sequence, candidate block), 256 threads; the CTA
+// reads key_length on the device, derives the past length P = K - L, and
+// exits at once if its block is not completed by this call (no host sync).
+// Threads are laid out as (row group g, 16-byte channel chunk c): every
+// thread keeps kbs/G independent 16-byte loads in flight, sums them in
+// float32, and the G partial rows are reduced in shared memory. The mean,
+// the block-wide sum of squares, the rotation and one rounding to the
+// output type follow; the 2*Di-byte key row is written once. One extra CTA
+// per sequence writes the optional carry outputs.
+#include "kvr_internal.cuh"
+
+namespace kvr {
+
+constexpr int QSA_THREADS = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float x = threadIdx.x < QSA_THREADS / 32 ? red[threadIdx.x] : 0.f;
+        x = warp_sum(x);
+        if (threadIdx.x == 0) red[QSA_THREADS / 32] = x;
+    }
+    __syncthreads();
+    return red[QSA_THREADS / 32];
+}
+
+template <class IT, int VW>
+__device__ __forceinline__ void accumulate(const uint16_t* src, float* acc) {
+    if constexpr (VW == 8) {
+        const uint4 v = ld_stream_v4(src);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc[2 * k] += IT::lo(w[k]);
+            acc[2 * k + 1] += IT::hi(w[k]);
+        }
+    } else {
+        acc[0] += IT::one(*src);
+    }
+}
+
+template <class IT, int VW>
+__global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
+    extern __shared__ __align__(16) float sm[];
+    const int tid = threadIdx.x;
+    const int64_t per_seq = p.nbmax + 1;
+    const int64_t n = int64_t(blockIdx.x) / per_seq;
+    const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
+
+    const int64_t K = p.key_length[p.key_length_per_seq ? n : 0];
+    const int64_t P = K - p.L;
+    if (P < 0) {
+        if (jl == 0 && tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_KEY_LENGTH);
+        return;
+    }
+    const int64_t kbs = p.kbs;
+    const int64_t F = P - P % kbs;            // first token of the incomplete block
+    const int64_t j0 = P / kbs;
+    const int64_t nb = K / kbs - j0;          // blocks completed by this call
+    const int Di = p.Di;
+    const uint16_t* raw = static_cast<const uint16_t*>(p.raw) + n * p.L * Di;
+    const uint16_t* past = static_cast<const uint16_t*>(p.past_raw) + n * (kbs - 1) * Di;
+
+    if (jl == p.nbmax) {
+        // ---- carry outputs: tokens after the last completed block ----
+        const int64_t Fn = (K / kbs) * kbs;
+        const int64_t rem = K - Fn;
+        if (p.next_raw != nullptr) {
+            uint16_t* dst = static_cast<uint16_t*>(p.next_raw) + n * (kbs - 1) * Di;
+            for (int64_t e = tid; e < rem * Di; e += QSA_THREADS) {
+                const int64_t r = e / Di, ch = e - r * Di;
+                const int64_t tok = Fn + r;
+                dst[e] = tok < P ? past[(tok - F) * Di + ch] : raw[(tok - P) * Di + ch];
+            }
+        }
+        if (p.next_rope != nullptr && p.Dr > 0 && rem > 0) {
+            uint16_t* dst = static_cast<uint16_t*>(p.next_rope) + n * 2 * p.Dr;
+            for (int e = tid; e < 2 * p.Dr; e += QSA_THREADS) {
+                uint16_t v;
+                if (Fn >= P) {
+                    const int64_t row = (n * p.L + (Fn - P)) * p.Dr;
+                    v = e < p.Dr ? static_cast<const uint16_t*>(p.cos)[row + e]
+                                 : static_cast<const uint16_t*>(p.sin)[row + e - p.Dr];
+                } else {
+                    v = static_cast<const uint16_t*>(p.past_rope)[n * 2 * p.Dr + e];
+                }
+                dst[e] = v;
+            }
+        }
+        return;
+    }
+    if (jl >= nb) return;
+    const int64_t j = j0 + jl;
+    if (j >= p.Bcap) {
+        if (tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_BLOCK_CAP);
+        return;
+    }
+    const int64_t tok0 = j * kbs;
+
+    // ---- block sum: thread (g, c) sums rows g, g+G, ... of chunk c ----
+    const int C = Di / VW;
+    const int G = C >= QSA_THREADS ? 1 : QSA_THREADS / C;
+    float* part = sm;                 // [G][Di]
+    float* u = sm + G * Di;           // [Di]
+    float* red = u + Di;              // [QSA_THREADS/32 + 1]
+    for (int cbase = 0; cbase < (C > QSA_THREADS ? C : 1); cbase += QSA_THREADS) {
+        const int c = C >= QSA_THREADS ? cbase + tid : tid % C;
+        const int g = C >= QSA_THREADS ? 0 : tid / C;
+        if (c < C && g < G) {
+            float acc[VW];
+#pragma unroll
+            for (int k = 0; k < VW; ++k) acc[k] = 0.f;
+#pragma unroll 4
+            for (int64_t r = g; r < kbs; r += G) {
+                const int64_t tok = tok0 + r;
+                const uint16_t* src = tok < P ? past + (tok - F) * Di : raw + (tok - P) * Di;
+                accumulate<IT, VW>(src + c * VW, acc);
+            }
+#pragma unroll
+            for (int k = 0; k < VW; ++k) part[g * Di + c * VW + k] = acc[k];
+        }
+    }
+    __syncthreads();
+
+    // ---- mean, optional RMS normalisation ----
+    float ss = 0.f;
+    for (int ch = tid; ch < Di; ch += QSA_THREADS) {
+        float s = 0.f;
+        for (int g = 0; g < G; ++g) s += part[g * Di + ch];
+        const float m = s / float(kbs);
+        u[ch] = m;
+        ss = fmaf(m, m, ss);
+    }
+    if (p.w != nullptr) {
+        const float tot = block_sum(ss, red);
+        const float rr = rsqrtf(fmaf(tot, p.inv_di, p.eps));
+        const uint16_t* w = static_cast<const uint16_t*>(p.w);
+        for (int ch = tid; ch < Di; ch += QSA_THREADS) u[ch] = u[ch] * rr * IT::one(w[ch]);
+    }
+    __syncthreads();
+
+    // ---- rotation of the last Dr channels with the first token's RoPE, write ----
+    const uint16_t* cr = nullptr;
+    const uint16_t* sr = nullptr;
+    if (p.Dr > 0) {
+        if (tok0 >= P) {
+            cr = static_cast<const uint16_t*>(p.cos) + (n * p.L + (tok0 - P)) * p.Dr;
+            sr = static_cast<const uint16_t*>(p.sin) + (n * p.L + (tok0 - P)) * p.Dr;
+        } else {
+            cr = static_cast<const uint16_t*>(p.past_rope) + n * 2 * p.Dr;
+            sr = cr + p.Dr;
+        }
+    }
+    const int base = Di - p.Dr;
+    const int h = p.Dr >> 1;
+    uint16_t* out = static_cast<uint16_t*>(p.block_keys) + (n * p.Bcap + j) * Di;
+    for (int ch = tid; ch < Di; ch += QSA_THREADS) {
+        float v;
+        if (ch < base) {
+            v = u[ch];
+        } else {
+            const int i = ch - base;              // table lane in [0, Dr)
+            const int q = i < h ? i : i - h;      // pair index
+            const float a = u[base + 2 * q];      // x1 = even lane
+            const float b = u[base + 2 * q + 1];  // x2 = odd lane
+            const float c = IT::one(cr[i]);
+            const float s = IT::one(sr[i]);
+            v = i < h ? a * c - b * s : b * c + a * s;
+        }
+        out[ch] = IT::one_out(v);
+    }
+}
+
+cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, cudaStream_t s) {
+    const int C = vec ? p.Di / 8 : p.Di;
+    const int G = C >= QSA_THREADS ? 1 : QSA_THREADS / C;
+    const size_t smem = (size_t(G) * p.Di + p.Di + QSA_THREADS / 32 + 1) * sizeof(float);
+    const int64_t grid = p.N * (p.nbmax + 1);
+    if (vec) {
+        auto fn = in_dtype == KVR_BF16 ? qsa_kernel<BF16, 8> : qsa_kernel<F16, 8>;
+        fn<<<unsigned(grid), QSA_THREADS, smem, s>>>(p);
+    } else {
+        auto fn = in_dtype == KVR_BF16 ? qsa_kernel<BF16, 1> : qsa_kernel<F16, 1>;
+        fn<<<unsigned(grid), QSA_THREADS, smem, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -158,7 +158,7 @@ def make_kv_case(name, Bkv, Skv, Dv=512, Dk=64, mode="PA_BSND", d0=None, d1=128,
                   cos=cos, sin=sin, index=index, ckv_scale=ckv_scale, k_scale=k_scale,
                   kc_scale=kc_scale, meta=dict(seed=seed, kv_std=kv_std, pos=pos,
                                                slots=slots, skip=skip, in_dtype=in_dtype,
-                                               row_pad=row_pad))
+                                               row_pad=row_pad, wide=wide))
 
 
 # The five synthetic workloads (seed = 1000 + workload number).
@@ -265,3 +265,25 @@ KV_WORKLOADS = {
     "prefill_paged": prefill_paged,
     "quant_fp8": quant_fp8,
 }
+
+
+def decode_paged_sets(n_sets, seed=1002, Bkv=256, Dv=512, Dk=64, block_num=4096, block_size=128,
+                      n_skip=5, pos_max=32768):
+    """`n_sets` independent decode batches shaped like decode_paged, stacked:
+    kv [n, Bkv, 1, 1, Dv+Dk], cos/sin [n, Bkv, 1, 1, Dk], index [n, Bkv] and
+    one gamma [Dv]. All slots are distinct (within and across sets); n_skip
+    entries per set are -1. Used to rotate a benchmark's inputs through more
+    memory than L2 holds."""
+    g = torch.Generator().manual_seed(seed)
+    D = Dv + Dk
+    kv = (torch.randn(n_sets, Bkv, 1, 1, D, generator=g, dtype=torch.float32)).to(torch.bfloat16)
+    gamma = (torch.rand(Dv, generator=g, dtype=torch.float32) + 0.5).to(torch.bfloat16)
+    pos = torch.randint(0, pos_max, (n_sets, Bkv), generator=g)
+    cos, sin = rope_tables(pos, Dk)
+    slots = torch.randperm(block_num * block_size, generator=g)[:n_sets * Bkv].view(n_sets, Bkv).clone()
+    if n_skip:
+        drop = torch.rand(n_sets, Bkv, generator=g).argsort(dim=1)[:, :n_skip]
+        slots.scatter_(1, drop, -1)
+    return dict(kv=kv, gamma=gamma, cos=cos.view(n_sets, Bkv, 1, 1, Dk),
+                sin=sin.view(n_sets, Bkv, 1, 1, Dk), index=slots.to(torch.int64),
+                Dv=Dv, Dk=Dk, d0=block_num, d1=block_size)

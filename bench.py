@@ -1,0 +1,570 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused KV prologue (RMSNorm + interleaved RoPE + paged
+cache scatter) on the decode workload, plus the other workloads as extras.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one kv_rmsnorm_rope_cache call on one decode batch: Bkv = 256
+tokens, Skv = 1, D = 512 + 64 bf16, PA_BSND cache BlockSize 128 x BlockNum
+4096, 5 of 256 index entries -1. Steps rotate over 512 independent input
+sets (185 MB > L2), so every step reads its inputs from HBM. The K timed
+steps run as CUDA-graph replays of back-to-back calls (a graph of one
+512-step rotation, replayed, plus a remainder graph), timed with CUDA events
+on the capture stream. With N > 1 (torchrun) each rank runs an independent
+replica on its own GPU; the job value sums tokens over ranks and divides by
+the slowest rank's time (weak scaling, no data-path collective).
+
+Printed on rank 0: one JSON line with the metric, the roofline of the kernel,
+the CPU oracle baseline, the end-to-end figure (host buffers, host<->device
+copies inside the timed region), clocks sampled during the timed region, and
+the other workloads (prefill, FP8 quantised, QSA prepare) under "extras".
+"""
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and achieved HBM GB/s (% of GB300 peak) for fused norm+RoPE+cache write"
+UNIT = "tokens/s"
+ROTATION = 512           # input sets rotated through by the decode steps
+DEFAULT_STEPS = 102400   # 200 rotations, ~0.3 s of GPU time
+DEFAULT_WARMUP = 1024
+WORKLOAD = ("decode_paged: Bkv=256 Skv=1 N=1 D=576 (Dv=512 rmsnorm, Dk=64 interleaved RoPE) bf16, "
+            "kv ~N(0,1), gamma ~U(0.5,1.5), positions ~U[0,32768), PA_BSND bf16 caches "
+            "BlockSize=128 BlockNum=4096, 256 distinct slots per batch with 5 (2%) set to -1")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kv_rmsnorm_rope_cache__decode_paged.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "attention_prologue_kv_gb300", "csrc", f)
+                  for f in ("kv_rmsnorm_rope_cache.cu", "kvr_internal.cuh")]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=DEFAULT_STEPS)
+    ap.add_argument("--warmup", type=int, default=DEFAULT_WARMUP)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline leg")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    a = ap.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+    a.steps = max(a.steps, 1)
+    return a
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes (what the method must move; untouched cache slots and
+# -1 rows' inputs are not counted)
+# ---------------------------------------------------------------------------
+
+def kv_algorithmic_bytes(n_active, n_skipped, Dv=512, Dk=64, in_bytes=2, ckv_bytes=2, k_bytes=2,
+                         scale_bytes=0):
+    per_active = (Dv + Dk) * in_bytes + 2 * Dk * in_bytes + 8 + Dv * ckv_bytes + Dk * k_bytes
+    return n_active * per_active + n_skipped * 8 + Dv * in_bytes + scale_bytes
+
+
+def qsa_algorithmic_bytes(n_blocks, n_seq, kbs, Di, Dr, in_bytes=2):
+    per_block = kbs * Di * in_bytes + 2 * Dr * in_bytes + Di * in_bytes
+    return n_blocks * per_block + n_seq * 8 + Di * in_bytes
+
+
+# ---------------------------------------------------------------------------
+# Multi-rank plumbing (replicas: only the timing result is exchanged)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_timing(elapsed_ms, tokens, device=None):
+    """Max of the elapsed time and sum of the tokens over all ranks (identity
+    when no process group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(elapsed_ms), float(tokens)
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                    "-lms", "50", "-i", str(gpu_id)]
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        if self.p is None:
+            return None
+        time.sleep(0.15)
+        self.p.terminate()
+        try:
+            out = self.p.communicate(timeout=10)[0]
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out = self.p.communicate()[0]
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.06 <= r[0] <= t1 + 0.06]
+        window = "timed region"
+        if not inside:
+            inside = rows
+            window = "whole run (timed region shorter than the sampling interval)"
+        reasons = sorted({self.REASONS[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def gpu_smi_id(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return dev
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    try:
+        lines = open(PROFILE_SUMMARY).read().splitlines()
+    except OSError:
+        return None, None
+    kv = {}
+    for line in lines:
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            kv[k.strip()] = v.strip().strip("`")
+    if kv.get("kernel_source_sha256") != kernel_source_hash():
+        return None, "stale"
+    try:
+        return float(kv["traffic_bytes_per_launch"]), "ok"
+    except (KeyError, ValueError):
+        return None, None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def l2_flush(buf):
+    buf.add_(1)
+
+
+def time_each(fn, n, flush, stream):
+    """Median/min of n single-launch durations (CUDA events on `stream`), L2 flushed before each."""
+    import torch
+    ts = []
+    for _ in range(n):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts), min(ts)
+
+
+def cpu_oracle_baseline(budget_s, sets, d0, d1):
+    """The oracle as it stands, on decode batches of the same workload, for
+    about budget_s seconds of single-process CPU time. Returns tokens/s."""
+    import numpy as np
+    import torch
+
+    import oracle
+    ckv = np.full((d0, d1, 512), 0x7FBF, dtype=np.uint16)
+    kc = np.full((d0, d1, 64), 0x7FBF, dtype=np.uint16)
+    gamma = sets["gamma"].to(torch.float64).numpy()
+    n_tok, n_batch = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        i = n_batch % sets["kv"].shape[0]
+        kv = sets["kv"][i].double().numpy().reshape(1, -1, 576).transpose(1, 0, 2)
+        cos = sets["cos"][i].double().numpy().reshape(-1, 1, 64)
+        sin = sets["sin"][i].double().numpy().reshape(-1, 1, 64)
+        oracle.ref_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, sets["index"][i].numpy(), ckv, kc,
+                                         Dv=512, mode="PA_BSND", eps=1e-6)
+        n_tok += kv.shape[0]
+        n_batch += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return n_tok / el, n_batch, el
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import attention_prologue_kv_gb300 as kvr
+    from attention_prologue_kv_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    from attention_prologue_kv_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    barrier()
+
+    # ---- inputs: ROTATION decode batches resident in HBM ----
+    sets = wl.decode_paged_sets(ROTATION, seed=1002 + 100003 * rank)
+    R = ROTATION
+    kv = sets["kv"].to(dev)
+    cos = sets["cos"].to(dev)
+    sin = sets["sin"].to(dev)
+    index = sets["index"].to(dev)
+    gamma = sets["gamma"].to(dev)
+    d0, d1 = sets["d0"], sets["d1"]
+    ckv = torch.full((d0, d1, 1, 512), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    kc = torch.full((d0, d1, 1, 64), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_skip = (sets["index"] == -1).sum(dim=1)
+    Bkv = kv.shape[1]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def step(i):
+        kvr.kv_rmsnorm_rope_cache(kv[i], gamma, cos[i], sin[i], index[i], ckv, kc,
+                                  cache_mode="PA_BSND", eps=1e-6, dev_status=status)
+
+    # ---- warm-up: W eager steps ----
+    for w in range(args.warmup):
+        step((R - 1 - w) % R)
+    torch.cuda.synchronize()
+
+    # ---- graphs: one full rotation, plus the remainder ----
+    K = args.steps
+    full, rem = divmod(K, R)
+    g_full = g_rem = None
+    if full:
+        g_full = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_full):
+            for i in range(R):
+                step(i)
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem):
+            for i in range(rem):
+                step(i)
+    if g_full is not None:
+        g_full.replay()      # one untimed replay: graph upload and first-launch costs
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    sampler = ClockSampler(gpu_smi_id(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    l2_flush(flush_buf)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record(stream)
+    for _ in range(full):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    clocks = sampler.stop(wall0, wall1) if sampler else None
+    assert int(status.item()) == 0, "device status %d" % int(status.item())
+
+    tokens = Bkv * K
+    job_ms, job_tokens = reduce_timing(elapsed_ms, tokens, dev)
+    value = job_tokens / (job_ms / 1e3)
+
+    # per-launch algorithmic bytes, averaged over the sets the K steps used
+    used = [i % R for i in range(K)] if K < R else list(range(R))
+    skips = [int(n_skip[i]) for i in used]
+    avg_bytes = statistics.fmean(kv_algorithmic_bytes(Bkv - s, s) for s in skips)
+    per_launch_s = elapsed_ms / 1e3 / K
+    achieved = avg_bytes / per_launch_s / 1e9
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    traffic, traffic_state = profiled_traffic()
+
+    result = None
+    if rank == 0:
+        # ---- end to end: host buffers, one packed H2D copy per step, status read back ----
+        e2e = e2e_decode(args, sets, gamma, ckv, kc, dev, kvr)
+        extras = None if args.no_extras else run_extras(dev, kvr, wl, flush_buf)
+        cpu_tps, n_batches, cpu_s = cpu_oracle_baseline(args.cpu_seconds, sets, d0, d1)
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": job_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD,
+                       "step": "one kv_rmsnorm_rope_cache call on one 256-token decode batch",
+                       "l2": "inputs larger than L2: steps rotate over %d input sets (%.0f MB > %.0f MB L2)"
+                             % (R, (kv.numel() + cos.numel() * 2) * 2 / 1e6 + index.numel() * 8 / 1e6, l2 / 1e6),
+                       "launch": "CUDA graph replays of back-to-back calls (%d x %d-step graph + %d-step graph)"
+                                 % (full, R, rem),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src,
+                         "bytes_per_launch": avg_bytes, "launch_us": per_launch_s * 1e6,
+                         "traffic_source": PROFILE_SUMMARY.replace(ROOT + "/", "") if traffic else traffic_state},
+            "cpu_baseline": {"value": cpu_tps, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "%d decode batches of 256 tokens (%.1f s, float64 NumPy, one process)"
+                                       % (n_batches, cpu_s)},
+            "e2e": e2e,
+            "gpu_launches": K,
+            "clocks": clocks,
+            "extras": extras,
+        }
+    if world > 1:
+        dist.destroy_process_group()
+    return result
+
+
+def e2e_decode(args, sets, gamma, ckv, kc, dev, kvr):
+    """Same metric through the public API with the inputs in pinned host
+    memory: per step one host->device copy of the packed batch, the call, and
+    a device->host read of the status word; timed over the K steps."""
+    import torch
+    R = sets["kv"].shape[0]
+    kvb = sets["kv"][0].numel() * 2
+    csb = sets["cos"][0].numel() * 2
+    ixb = sets["index"][0].numel() * 8
+    blob = kvb + 2 * csb + ixb
+    host = torch.empty(R, blob, dtype=torch.uint8).pin_memory()
+    host[:, :kvb] = sets["kv"].reshape(R, -1).view(torch.uint8)
+    host[:, kvb:kvb + csb] = sets["cos"].reshape(R, -1).view(torch.uint8)
+    host[:, kvb + csb:kvb + 2 * csb] = sets["sin"].reshape(R, -1).view(torch.uint8)
+    host[:, kvb + 2 * csb:] = sets["index"].reshape(R, -1).view(torch.uint8)
+    stage = torch.empty(blob, dtype=torch.uint8, device=dev)
+    B = sets["kv"].shape[1]
+    kv_v = stage[:kvb].view(torch.bfloat16).view(B, 1, 1, -1)
+    cos_v = stage[kvb:kvb + csb].view(torch.bfloat16).view(B, 1, 1, -1)
+    sin_v = stage[kvb + csb:kvb + 2 * csb].view(torch.bfloat16).view(B, 1, 1, -1)
+    idx_v = stage[kvb + 2 * csb:].view(torch.int64)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    K = args.steps
+    st_host = torch.zeros(K, dtype=torch.int32).pin_memory()
+
+    def one(i, k):
+        stage.copy_(host[i], non_blocking=True)
+        kvr.kv_rmsnorm_rope_cache(kv_v, gamma, cos_v, sin_v, idx_v, ckv, kc, cache_mode="PA_BSND",
+                                  eps=1e-6, dev_status=status)
+        st_host[k:k + 1].copy_(status, non_blocking=True)
+
+    for w in range(min(args.warmup, 64)):
+        one(w % R, 0)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for k in range(K):
+        one(k % R, k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    assert int(st_host.max()) == 0
+    return {"value": B * K / wall, "unit": UNIT, "h2d_bytes_per_step": blob, "d2h_bytes_per_step": 4,
+            "device_ms": e0.elapsed_time(e1), "wall_ms": wall * 1e3,
+            "how": "public Python API, one packed pinned H2D copy + call + status D2H per step, one stream"}
+
+
+def run_extras(dev, kvr, wl, flush_buf):
+    """The other workloads, each timed per launch with L2 flushed before it."""
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream()
+    flush = lambda: l2_flush(flush_buf)
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs", 6800.0)
+
+    # in-process copy reference (16-byte vectorised device copy, 2 x 512 MB)
+    src = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    med, best = time_each(lambda: kvr.device_copy(dst, src), 10, flush, stream)
+    copy_gbs = 2 * src.numel() / (best / 1e3) / 1e9
+    out["copy_peak_gbs_in_run"] = copy_gbs
+    del src, dst
+
+    def kv_case(case):
+        D = case.Dv + case.Dk
+        kv = case.kv.to(dev)
+        ckv = torch.zeros(case.cache_shapes()[0], dtype=wl.code_torch_dtype(case.ckv_dtype), device=dev).view(
+            wl.TORCH_DTYPES[case.ckv_dtype])
+        kc = torch.zeros(case.cache_shapes()[1], dtype=wl.code_torch_dtype(case.k_dtype), device=dev).view(
+            wl.TORCH_DTYPES[case.k_dtype])
+        args = (kv, case.gamma.to(dev), case.cos.to(dev), case.sin.to(dev), case.index.to(dev), ckv, kc)
+        kw = dict(cache_mode=case.mode, eps=case.eps,
+                  ckv_scale=None if case.ckv_scale is None else case.ckv_scale.to(dev))
+        fn = lambda: kvr.kv_rmsnorm_rope_cache(*args, **kw)
+        for _ in range(3):
+            fn()
+        med, best = time_each(fn, 20, flush, stream)
+        act = case.active_tokens()
+        nbytes = kv_algorithmic_bytes(act, case.T - act, case.Dv, case.Dk,
+                                      ckv_bytes=1 if case.ckv_dtype != "bf16" else 2,
+                                      scale_bytes=0 if case.ckv_scale is None else 4 * case.ckv_scale.numel())
+        gbs = nbytes / (med / 1e3) / 1e9
+        return {"tokens": case.T, "us_median": med * 1e3, "us_min": best * 1e3,
+                "tokens_per_s": case.T / (med / 1e3), "bytes": nbytes, "gbs": gbs,
+                "frac_of_measured_peak": gbs / peak, "frac_of_copy_in_run": gbs / copy_gbs,
+                "frac_of_nominal_8000": gbs / 8000.0}
+
+    out["prefill_paged"] = kv_case(wl.prefill_paged())
+    out["quant_fp8"] = kv_case(wl.quant_fp8())
+    out["tiny_norm"] = kv_case(wl.tiny_norm())
+
+    q = wl.qsa_prepare_workload()
+    bk = torch.zeros(q.N, q.Bcap, q.Di, dtype=torch.bfloat16, device=dev)
+    d = lambda t: t.to(dev)
+    qargs = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
+             d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
+    fn = lambda: kvr.qsa_prepare(*qargs)
+    for _ in range(3):
+        fn()
+    med, best = time_each(fn, 20, flush, stream)
+    nb = q.completed_blocks()
+    nbytes = qsa_algorithmic_bytes(nb, q.N, q.kbs, q.Di, q.Dr)
+    gbs = nbytes / (med / 1e3) / 1e9
+    out["qsa_prepare"] = {"new_tokens": q.N * q.L, "blocks": nb, "us_median": med * 1e3, "us_min": best * 1e3,
+                          "new_tokens_per_s": q.N * q.L / (med / 1e3), "bytes": nbytes, "gbs": gbs,
+                          "frac_of_measured_peak": gbs / peak, "frac_of_copy_in_run": gbs / copy_gbs}
+    torch.cuda.synchronize()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    import numpy as np
+    import torch
+
+    import oracle
+    from attention_prologue_kv_gb300 import workloads as wl
+    sets = wl.decode_paged_sets(16, seed=1002)
+    d0, d1 = sets["d0"], sets["d1"]
+    ckv = np.full((d0, d1, 512), 0x7FBF, dtype=np.uint16)
+    kc = np.full((d0, d1, 64), 0x7FBF, dtype=np.uint16)
+    gamma = sets["gamma"].to(torch.float64).numpy()
+    B = sets["kv"].shape[1]
+
+    def batch(i, ntok):
+        kv = sets["kv"][i].double().numpy().reshape(-1, 1, 576)[:ntok]
+        cos = sets["cos"][i].double().numpy().reshape(-1, 1, 64)[:ntok]
+        sin = sets["sin"][i].double().numpy().reshape(-1, 1, 64)[:ntok]
+        oracle.ref_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, sets["index"][i].numpy()[:ntok], ckv, kc,
+                                         Dv=512, mode="PA_BSND", eps=1e-6)
+
+    t = time.perf_counter()
+    batch(0, B)
+    t_full = time.perf_counter() - t
+    budget = 120.0
+    ntok = B if (args.steps + args.warmup) * t_full <= budget else max(
+        1, int(B * budget / ((args.steps + args.warmup) * t_full)))
+    for w in range(args.warmup):
+        batch(w % 16, ntok)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        batch(k % 16, ntok)
+    el = time.perf_counter() - t0
+    value = ntok * args.steps / el
+    sample = "%d of 256 tokens of each decode batch per step, float64 NumPy oracle, one process" % ntok
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "step": "oracle on a bounded sample of one decode batch"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, _ = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    res = run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,226 @@
+/*
+ * kvr.h - C ABI of libkvr.so, the GB300 (sm_103a) attention-prologue key path.
+ *
+ * Two operations:
+ *
+ *   kv_rmsnorm_rope_cache()  the fused KV prologue of the page
+ *       "aclnnKvRmsNormRopeCache" (hiascend.com, CANN ops-transformer):
+ *       each token row of width D = Dv + Dk is split on its tail axis
+ *       ("Description"); the left Dv part is RMS-normalised
+ *       ("Formulas (2) rmsNorm": y = x / sqrt(mean(x^2) + eps) * gamma),
+ *       the right Dk part gets the interleaved RoPE ("Formulas (1)
+ *       interleaveRope": y = cat(x[::2], x[1::2]) * cos + cat(-x[1::2], x[::2]) * sin),
+ *       and both results are scattered by slot index into two caches
+ *       ("Restrictions on index"), optionally quantised to 8-bit codes
+ *       ("Restrictions on quantization scenarios"). The kcScale factor
+ *       alpha_kv of "aclnnMlaPrologV3WeightNz" ("Formula", key path) may
+ *       scale the normalised part.
+ *
+ *   qsa_prepare()  the block-key prepare of "openvino.opset17.qsa_prepare"
+ *       (docs.openvino.ai): one key per key block completed by the new
+ *       tokens = mean of the block's raw index keys, RMS-normalised with
+ *       k_norm_weight, rotated with the RoPE of the block's first token;
+ *       incomplete blocks are carried across calls.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates nothing and keeps no per-call state. Rows are dense
+ *     and row-major unless a stride argument says otherwise.
+ *   - Calls are asynchronous on `stream`: they validate on the host, launch,
+ *     and return. Nothing is read back to the host.
+ *   - Host-side errors (a NULL that is required, a bad shape, dtype or
+ *     mode) are returned before any launch; nothing is written.
+ *   - Data-dependent errors are found on the device: the offending row or
+ *     block is skipped (never written out of bounds) and, if `dev_status`
+ *     is non-NULL, the matching KVR_DEVERR_* bit is OR-ed into *dev_status.
+ *     No kernel traps, asserts or spins.
+ *   - An empty problem (T = Bkv*Skv = 0, or N*L = 0) returns KVR_OK with no
+ *     launch, mirroring the empty-tensor rule of "aclnnMlaPrologV3WeightNz"
+ *     ("Shape restrictions": caches are not updated).
+ *   - Results are deterministic: no atomics touch data.
+ *   - Thread safe: entry points may be called concurrently from any host
+ *     thread on any stream; overlapping writes to the same cache rows from
+ *     concurrent calls are the caller's race.
+ */
+#ifndef KVR_H
+#define KVR_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVR_ABI_VERSION 1
+
+typedef enum kvr_status {
+    KVR_OK = 0,
+    KVR_ERR_NULL = 1,         /* a required pointer is NULL, or optional pairs disagree */
+    KVR_ERR_SHAPE = 2,        /* a size is out of its documented range */
+    KVR_ERR_DTYPE = 3,        /* an element type is not supported for that argument */
+    KVR_ERR_MODE = 4,         /* unknown cache mode */
+    KVR_ERR_ALIAS = 5,        /* an output overlaps an input it must not overlap */
+    KVR_ERR_CUDA = 6          /* the launch failed (see cudaGetLastError) */
+} kvr_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define KVR_DEVERR_INDEX 0x1       /* kv: an index entry outside {-1} U [0, range) */
+#define KVR_DEVERR_KEY_LENGTH 0x2  /* qsa: key_length[n] < L (the past length would be negative) */
+#define KVR_DEVERR_BLOCK_CAP 0x4   /* qsa: a completed block's number is >= Bcap */
+
+typedef enum kvr_dtype {
+    KVR_BF16 = 0,
+    KVR_F16 = 1,
+    KVR_INT8 = 2,             /* caches only: round half to even, clamp to [-128, 127] */
+    KVR_FP8_E4M3FN = 3,       /* caches only: round to nearest even, saturate to +-448 */
+    KVR_FP8_E5M2 = 4          /* caches only: round to nearest even, saturate to +-57344 */
+} kvr_dtype;
+
+/* Cache layouts of "aclnnKvRmsNormRopeCache" ("Restrictions on index"); the
+ * head axis N is 1, so BNSD and BSND are the same bytes. */
+typedef enum kvr_cache_mode {
+    /* cache [Bcache=d0, Scache=d1, 1, D*]; index [Bkv, Skv] in [-1, Scache);
+     * token (b, s) goes to cache row (b, index[b, s]); requires Bcache >= Bkv. */
+    KVR_CACHE_NORM = 0,
+    /* cache [BlockNum=d0, BlockSize=d1, 1, D*]; index [Bkv*Skv] in
+     * [-1, BlockNum*BlockSize); token t goes to slot index[t]. */
+    KVR_CACHE_PA_BSND = 1,
+    /* cache as PA_BSND; index [Bkv * ceil(Skv/BlockSize)], one entry per
+     * BlockSize tokens of a sequence; token s goes to slot
+     * index[b, s / BlockSize] + s % BlockSize, which must stay inside the
+     * block the entry names (else KVR_DEVERR_INDEX). */
+    KVR_CACHE_PA_BLK_BSND = 2
+} kvr_cache_mode;
+
+/*
+ * Arguments of kv_rmsnorm_rope_cache(). T = Bkv * Skv token rows.
+ *
+ *   kv         [Bkv, 1, Skv, >= Dv+Dk] input rows, element type `in_dtype`
+ *              (bf16 or f16). Row t starts kv_row_stride elements after row
+ *              t-1 (0 means Dv+Dk, i.e. dense); a larger stride reads kv as
+ *              a column slice of a wider row (e.g. a fused projection output).
+ *   gamma      [Dv] RMSNorm weight, `in_dtype`.
+ *   cos, sin   [Bkv, 1, Skv, Dk] full-width RoPE tables, `in_dtype`; output
+ *              lane i < Dk/2 uses entry i, lane i + Dk/2 uses entry i + Dk/2.
+ *   index      int64, layout per `mode` (see kvr_cache_mode); -1 = skip.
+ *              Repeated targets within one call (forbidden by the page) leave
+ *              an unspecified winner.
+ *   cache_d0, cache_d1   the two leading cache dims (Bcache, Scache) or
+ *              (BlockNum, BlockSize).
+ *   ckv_cache  [d0, d1, 1, Dv] of `ckv_dtype`; k_cache [d0, d1, 1, Dk] of `k_dtype`.
+ *              A cache dtype is `in_dtype` (bf16/f16) or an 8-bit code type.
+ *   ckv_scale  float32 [ckv_scale_len], len Dv (per channel) or 1 (per
+ *              tensor); required iff ckv_dtype is an 8-bit type, else NULL.
+ *              The code written is encode(alpha_kv * y[c] * ckv_scale[c]).
+ *   k_scale    same for the k cache (len Dk or 1), applied to the RoPE output lane c.
+ *   eps        added to the mean square (>= 0).
+ *   kc_scale   alpha_kv, multiplies the normalised part; pass 1.0f for none.
+ *   dev_status optional int32 device word; KVR_DEVERR_INDEX is OR-ed in when
+ *              an index entry is out of range (that token is skipped).
+ *
+ * Limits: Dv >= 1, Dk >= 2 and even, Bkv, Skv >= 0, d0, d1 >= 1.
+ * All arithmetic is float32 with one rounding to the cache type.
+ */
+typedef struct kvr_kv_args {
+    const void* kv;
+    kvr_dtype in_dtype;
+    int64_t Bkv, Skv, Dv, Dk;
+    int64_t kv_row_stride;
+    const void* gamma;
+    const void* cos;
+    const void* sin;
+    const int64_t* index;
+    kvr_cache_mode mode;
+    int64_t cache_d0, cache_d1;
+    void* ckv_cache;
+    kvr_dtype ckv_dtype;
+    const float* ckv_scale;
+    int64_t ckv_scale_len;
+    void* k_cache;
+    kvr_dtype k_dtype;
+    const float* k_scale;
+    int64_t k_scale_len;
+    float eps;
+    float kc_scale;
+    int32_t* dev_status;
+} kvr_kv_args;
+
+kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);
+
+/*
+ * Arguments of qsa_prepare(). Inputs follow the parameter list of
+ * "openvino.opset17.qsa_prepare".
+ *
+ *   raw_index_keys  [N, L, Di] raw index key of every new token, `in_dtype`.
+ *   block_keys      [N, Bcap, Di] in/out, `in_dtype`: the block keys of
+ *                   earlier calls (past_block_index_keys) followed by room for
+ *                   new ones. Block j (tokens [j*kbs, (j+1)*kbs) of the
+ *                   sequence) is written at row j; no other row is touched.
+ *   key_length      int64 [N] or [1] (key_length_len = N or 1): valid key
+ *                   tokens of each sequence AFTER this call, so the past
+ *                   length is P = key_length - L (< 0: KVR_DEVERR_KEY_LENGTH,
+ *                   the sequence is skipped). A [1] value applies to all N.
+ *   rope_cos, rope_sin  [N, L, Dr] RoPE of every new token, or both NULL to
+ *                   disable the rotation. The rotation is the interleaved RoPE
+ *                   of "aclnnKvRmsNormRopeCache" on channels [Di-Dr, Di).
+ *   k_norm_weight   [Di] or NULL (NULL disables the RMS normalisation).
+ *   past_incomplete_raw_keys  [N, kbs-1, Di]: raw keys of the past tokens of
+ *                   the incomplete block (rows >= P mod kbs are never read).
+ *   past_incomplete_rope      [N, 2*Dr] = [cos | sin] of the incomplete
+ *                   block's first token; NULL iff rope_cos is NULL. Read only
+ *                   when P mod kbs > 0.
+ *   key_block_size  kbs > 1.   eps >= 0.
+ *   next_incomplete_raw_keys  optional out [N, kbs-1, Di]: raw keys of the
+ *                   tokens after the last completed block (K mod kbs rows;
+ *                   the other rows are left untouched).
+ *   next_incomplete_rope      optional out [N, 2*Dr]: [cos | sin] of the
+ *                   first of those tokens (untouched when K mod kbs = 0).
+ *                   The next_* outputs must not overlap any input
+ *                   (KVR_ERR_ALIAS), so two carry buffers alternate between calls.
+ *   dev_status      optional int32 device word (KVR_DEVERR_KEY_LENGTH,
+ *                   KVR_DEVERR_BLOCK_CAP).
+ *
+ * Limits: N, L >= 0; Di >= 1; 0 <= Dr <= Di, Dr even; Bcap >= 1.
+ * Mean, normalisation and rotation in float32, one rounding to `in_dtype`.
+ */
+typedef struct kvr_qsa_args {
+    const void* raw_index_keys;
+    kvr_dtype in_dtype;
+    int64_t N, L, Di;
+    void* block_keys;
+    int64_t Bcap;
+    const int64_t* key_length;
+    int64_t key_length_len;
+    const void* rope_cos;
+    const void* rope_sin;
+    int64_t Dr;
+    const void* k_norm_weight;
+    const void* past_incomplete_raw_keys;
+    const void* past_incomplete_rope;
+    int64_t key_block_size;
+    float eps;
+    void* next_incomplete_raw_keys;
+    void* next_incomplete_rope;
+    int32_t* dev_status;
+} kvr_qsa_args;
+
+kvr_status qsa_prepare(const kvr_qsa_args* args, cudaStream_t stream);
+
+/* Measurement helper (no counterpart on the pages): a 16-byte vectorised
+ * device-to-device copy of `bytes` bytes (a multiple of 16, both pointers
+ * 16-byte aligned), used to measure the achievable HBM bandwidth in the same
+ * process as the kernels above. */
+kvr_status kvr_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* kvr_status_string(kvr_status status);
+
+/* KVR_ABI_VERSION of the loaded library. */
+int kvr_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVR_H */

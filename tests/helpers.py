@@ -89,3 +89,85 @@ def run_oracle_qsa(case, block_keys=None, carry=False):
     st = oracle.ref_qsa_prepare(block_keys=block_keys, next_raw=nr, next_rope=npr,
                                 **oracle_qsa_inputs(case))
     return block_keys, nr, npr, st
+
+
+# ---------------------------------------------------------------------------
+# GPU side (public Python API of the package only)
+# ---------------------------------------------------------------------------
+
+def kv_to_device(case, dev="cuda"):
+    """The case's kv on the device, keeping a strided-row layout when the case has one."""
+    D = case.Dv + case.Dk
+    if case.meta.get("row_pad"):
+        return case.meta["wide"].to(dev)[:, :D]
+    return case.kv.to(dev)
+
+
+def sentinel_cache(shape, dtype, dev="cuda"):
+    from attention_prologue_kv_gb300.workloads import TORCH_DTYPES, code_torch_dtype, sentinel
+    return torch.full(shape, sentinel(dtype), dtype=code_torch_dtype(dtype), device=dev).view(TORCH_DTYPES[dtype])
+
+
+def run_gpu_kv(case, kv=None, ckv=None, k=None, dev="cuda"):
+    """Run the CUDA path on a KVCase; returns (ckv codes, k codes, status) as numpy/int."""
+    import attention_prologue_kv_gb300 as kvr
+    sh_ckv, sh_k = case.cache_shapes()
+    if ckv is None:
+        ckv = sentinel_cache(sh_ckv, case.ckv_dtype, dev)
+        k = sentinel_cache(sh_k, case.k_dtype, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kvr.kv_rmsnorm_rope_cache(
+        kv_to_device(case, dev) if kv is None else kv, case.gamma.to(dev), case.cos.to(dev),
+        case.sin.to(dev), case.index.to(dev), ckv, k, cache_mode=case.mode, eps=case.eps,
+        ckv_scale=None if case.ckv_scale is None else case.ckv_scale.to(dev),
+        k_scale=None if case.k_scale is None else case.k_scale.to(dev),
+        kc_scale=case.kc_scale, dev_status=status)
+    torch.cuda.synchronize()
+    return codes_of(ckv), codes_of(k), int(status.item())
+
+
+def compare_cache(gpu, ref, dtype, D):
+    """Bit-exact on every row the oracle left untouched; on written rows,
+    |gpu - ref| <= 2**-7 * |ref| + 1e-6 for 16-bit types, at most one code
+    apart on the ordered code line for 8-bit types. Returns (rows written,
+    fraction of written elements that are bit-identical)."""
+    from attention_prologue_kv_gb300.workloads import sentinel
+    from oracle import encoders as enc
+    g = gpu.reshape(-1, D)
+    r = ref.reshape(-1, D)
+    written = ~np.all(r == sentinel(dtype), axis=1)
+    untouched_ok = np.array_equal(g[~written], r[~written])
+    assert untouched_ok, "bytes outside the indexed rows changed (%d rows)" % int(
+        np.sum(~np.all(g[~written] == r[~written], axis=1)))
+    gw, rw = g[written], r[written]
+    if dtype in ("bf16", "f16"):
+        gv, rv = enc.decode(gw, dtype), enc.decode(rw, dtype)
+        err = np.abs(gv - rv)
+        bad = ~(err <= 2.0**-7 * np.abs(rv) + 1e-6)
+        assert not bad.any(), "%d elements out of tolerance, e.g. gpu %s ref %s" % (
+            int(bad.sum()), gv[bad][:4], rv[bad][:4])
+    else:
+        d = np.abs(enc.code_ordinal(gw, dtype) - enc.code_ordinal(rw, dtype))
+        assert d.max(initial=0) <= 1, "codes differ by %d" % int(d.max())
+    return int(written.sum()), float(np.mean(gw == rw)) if gw.size else 1.0
+
+
+def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda"):
+    import attention_prologue_kv_gb300 as kvr
+    from attention_prologue_kv_gb300.workloads import SENTINEL16
+    bk = block_keys
+    if bk is None:
+        bk = torch.full((case.N, case.Bcap, case.Di), SENTINEL16, dtype=torch.int16,
+                        device=dev).view(case.raw.dtype)
+    nr = npr = None
+    if carry:
+        nr = torch.full((case.N, case.kbs - 1, case.Di), float("nan"), dtype=case.raw.dtype, device=dev)
+        if case.Dr:
+            npr = torch.full((case.N, 2 * case.Dr), float("nan"), dtype=case.raw.dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    d = lambda t: None if t is None else t.to(dev)
+    kvr.qsa_prepare(d(case.raw), bk, d(case.key_length), d(case.rope_cos), d(case.rope_sin),
+                    d(case.k_norm_weight), d(case.past_raw), d(case.past_rope), case.kbs, case.eps,
+                    next_incomplete_raw_keys=nr, next_incomplete_rope=npr, dev_status=status)
+    torch.cuda.synchronize()
+    return codes_of(bk), f64(nr), f64(npr), int(status.item())

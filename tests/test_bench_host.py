@@ -1,0 +1,58 @@
+"""Host logic of the benchmark without a GPU: the algorithmic byte model and
+the replica timing reduction over two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_algorithmic_bytes_match_the_hand_count():
+    # decode: 251 active tokens x (1152 kv + 256 cos/sin + 8 index + 1024 ckv + 128 k) + 5 x 8 + 1024 gamma
+    assert bench.kv_algorithmic_bytes(251, 5) == 251 * 2568 + 40 + 1024 == 645632
+    # prefill: 32768 tokens, no skips
+    assert bench.kv_algorithmic_bytes(32768, 0) == 84149248
+    # FP8 ckv: 512-byte rows, plus the 2048-byte per-channel scale
+    assert bench.kv_algorithmic_bytes(4096, 0, ckv_bytes=1, scale_bytes=2048) == 4096 * 2056 + 1024 + 2048
+    # QSA: 32 sequences x 32 blocks x (64 rows x 256 B + 256 B cos/sin + 256 B key) + 32 x 8 + 256
+    assert bench.qsa_algorithmic_bytes(1024, 32, 64, 128, 64) == 17302016
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms, tok = bench.reduce_timing(10.0 + 5 * rank, 1000 * (rank + 1))
+        bench.barrier()
+        out[rank] = (ms, tok)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replica_timing_reduction_two_ranks():
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(2, _free_port(), out), nprocs=2, start_method="spawn")
+    assert out[0] == out[1] == (15.0, 3000.0)
+
+
+def test_reduce_timing_without_process_group_is_identity():
+    assert bench.reduce_timing(3.5, 42) == (3.5, 42.0)
+
+
+def test_default_arguments_obey_the_contract():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.impl == "ours"
+    assert bench.parse_args(["--warmup", "0"]).warmup == 3

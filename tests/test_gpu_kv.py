@@ -1,0 +1,164 @@
+"""GPU parity of kv_rmsnorm_rope_cache against the float64 oracle on the same
+seeded inputs: every cache byte outside the indexed rows bit-exact, 16-bit
+outputs within 2**-7*|ref| + 1e-6, 8-bit codes within one code; device
+status bits equal. Covers the four KV workloads at full size, both kernel
+paths (vectorised and generic), every cache mode and code type, strided and
+misaligned rows, and the degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+from attention_prologue_kv_gb300 import workloads as wl
+from helpers import compare_cache, run_gpu_kv, run_oracle_kv, sentinel_cache
+
+pytestmark = pytest.mark.gpu
+
+
+def check(case, **kw):
+    ref_ckv, ref_k, ref_st = run_oracle_kv(case)
+    g_ckv, g_k, g_st = run_gpu_kv(case, **kw)
+    assert g_st == ref_st
+    n1, ex1 = compare_cache(g_ckv, ref_ckv, case.ckv_dtype, case.Dv)
+    n2, ex2 = compare_cache(g_k, ref_k, case.k_dtype, case.Dk)
+    assert n1 == n2
+    return n1, ex1, ex2
+
+
+@pytest.mark.parametrize("make", [wl.tiny_norm, wl.decode_paged, wl.prefill_paged, wl.quant_fp8],
+                         ids=["tiny_norm", "decode_paged", "prefill_paged", "quant_fp8"])
+def test_workloads_full_size(make):
+    case = make()
+    n, ex_ckv, ex_k = check(case)
+    assert n == case.active_tokens()
+    # one rounding on each side: nearly every element is bit-identical
+    assert ex_ckv > 0.97 and ex_k > 0.97
+
+
+@pytest.mark.parametrize("Dv,Dk", [(512, 64), (24, 16), (256, 8), (1024, 256), (520, 72),
+                                   (6, 2), (1032, 64), (512, 258), (10, 6), (1, 2)])
+def test_shapes_vector_and_generic_paths(Dv, Dk):
+    case = wl.make_kv_case("s", 3, 37, Dv=Dv, Dk=Dk, mode="PA_BSND", d0=40, d1=4, seed=Dv * 7 + Dk,
+                           skip=5)
+    check(case)
+
+
+@pytest.mark.parametrize("mode", ["Norm", "PA_BSND", "PA_BLK_BSND"])
+@pytest.mark.parametrize("d1", [1, 3, 128])
+def test_cache_modes_ragged(mode, d1):
+    T_B, T_S = 5, 203
+    d0 = {"Norm": 7, "PA_BSND": -(-T_B * T_S // d1) + 3, "PA_BLK_BSND": T_B * -(-T_S // d1) + 2}[mode]
+    if mode == "Norm":
+        d1 = max(d1, T_S) + 1
+    case = wl.make_kv_case("m", T_B, T_S, mode=mode, d0=d0, d1=d1, seed=31 + d1, skip=3)
+    check(case)
+
+
+@pytest.mark.parametrize("ckv,k", [("int8", "bf16"), ("fp8_e4m3fn", "bf16"), ("fp8_e5m2", "bf16"),
+                                   ("bf16", "int8"), ("bf16", "fp8_e4m3fn"), ("bf16", "fp8_e5m2"),
+                                   ("int8", "int8"), ("fp8_e4m3fn", "fp8_e4m3fn"),
+                                   ("fp8_e5m2", "fp8_e4m3fn")])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quantisation_scenarios(ckv, k, per_tensor):
+    kw = dict(scale_len=1, k_scale_len=1) if per_tensor else {}
+    case = wl.make_kv_case("q", 16, 33, mode="PA_BSND", d0=8, d1=128, ckv_dtype=ckv, k_dtype=k,
+                           seed=41, skip=4, kv_std=3.0, **kw)
+    check(case)
+
+
+def test_quantisation_generic_path():
+    case = wl.make_kv_case("q", 4, 9, Dv=20, Dk=6, mode="PA_BSND", d0=4, d1=16,
+                           ckv_dtype="fp8_e4m3fn", k_dtype="int8", seed=42)
+    check(case)
+
+
+def test_fp16_inputs_and_caches():
+    case = wl.make_kv_case("h", 6, 50, mode="Norm", d0=8, d1=64, ckv_dtype="f16", k_dtype="f16",
+                           in_dtype="f16", seed=43, skip=7)
+    check(case)
+    case = wl.make_kv_case("h", 6, 50, mode="PA_BSND", d0=8, d1=64, ckv_dtype="fp8_e4m3fn",
+                           k_dtype="f16", in_dtype="f16", seed=44)
+    check(case)
+
+
+def test_kc_scale():
+    case = wl.make_kv_case("a", 4, 64, mode="PA_BSND", d0=4, d1=64, seed=45, kc_scale=0.3)
+    check(case)
+    case = wl.make_kv_case("a", 4, 64, mode="PA_BSND", d0=4, d1=64, seed=46, kc_scale=2.5,
+                           ckv_dtype="fp8_e4m3fn")
+    check(case)
+
+
+@pytest.mark.parametrize("pad", [64, 3])
+def test_strided_rows(pad):
+    """kv as a column slice of wider rows (vectorised when the stride keeps 16-byte rows)."""
+    case = wl.make_kv_case("w", 7, 40, mode="PA_BSND", d0=4, d1=128, seed=47, row_pad=pad)
+    assert not case.kv.is_contiguous()
+    check(case)
+
+
+def test_misaligned_pointers_take_the_generic_path():
+    case = wl.make_kv_case("u", 5, 11, mode="PA_BSND", d0=2, d1=64, seed=48)
+    T, D = case.T, case.Dv + case.Dk
+    buf = torch.empty(T * D + 1, dtype=torch.bfloat16, device="cuda")
+    kv = buf[1:].view(case.Bkv, 1, case.Skv, D)
+    kv.copy_(case.kv.cuda())
+    assert kv.data_ptr() % 16 != 0
+    check(case, kv=kv)
+
+
+def test_out_of_range_indices_are_skipped_and_flagged():
+    case = wl.make_kv_case("r", 4, 32, mode="PA_BSND", d0=8, d1=16, seed=49)
+    case.index[3] = 8 * 16
+    case.index[17] = -5
+    case.index[30] = 1 << 40
+    ref_ckv, ref_k, ref_st = run_oracle_kv(case)
+    assert ref_st == 1
+    n, _, _ = check(case)
+    assert n == 32 - 3
+
+
+def test_all_skipped_and_empty():
+    case = wl.make_kv_case("e", 3, 5, mode="PA_BSND", d0=2, d1=16, seed=50)
+    case.index[:] = -1
+    n, _, _ = check(case)
+    assert n == 0
+    case = wl.make_kv_case("e", 0, 5, mode="PA_BSND", d0=2, d1=16, seed=50)
+    g_ckv, g_k, st = run_gpu_kv(case)
+    assert st == 0 and np.all(g_ckv == wl.SENTINEL16) and np.all(g_k == wl.SENTINEL16)
+
+
+def test_norm_mode_with_larger_cache_batch_and_shared_slots():
+    """Norm indices may repeat across batches: each batch owns its cache row."""
+    case = wl.make_kv_case("n", 3, 10, mode="Norm", d0=5, d1=10, seed=51)
+    case.index[:] = torch.arange(10).flip(0)
+    check(case)
+
+
+def test_repeated_calls_overwrite_only_their_rows():
+    """Two calls into the same caches: the second overwrites its own rows only."""
+    a = wl.make_kv_case("c", 4, 16, mode="PA_BSND", d0=16, d1=16, seed=52)
+    b = wl.make_kv_case("c", 4, 16, mode="PA_BSND", d0=16, d1=16, seed=53)
+    ckv = sentinel_cache((16, 16, 1, 512), "bf16")
+    k = sentinel_cache((16, 16, 1, 64), "bf16")
+    run_gpu_kv(a, ckv=ckv, k=k)
+    g_ckv, g_k, st = run_gpu_kv(b, ckv=ckv, k=k)
+    r_ckv, r_k, _ = run_oracle_kv(a)
+    run_oracle_kv(b, r_ckv, r_k)
+    compare_cache(g_ckv, r_ckv, "bf16", 512)
+    compare_cache(g_k, r_k, "bf16", 64)
+
+
+def test_large_ragged_grid_stride():
+    """More rows than the grid holds at once, with a ragged tail."""
+    case = wl.make_kv_case("g", 3, 9001, mode="PA_BSND", d0=300, d1=128, seed=54, skip=101)
+    check(case)
+
+
+def test_rope_identity_on_gpu_is_exact_deinterleave():
+    case = wl.make_kv_case("i", 2, 8, mode="PA_BSND", d0=1, d1=16, seed=55)
+    case.cos[:] = 1.0
+    case.sin[:] = 0.0
+    _, g_k, _ = run_gpu_kv(case)
+    x = case.kv.reshape(-1, 576)[:, 512:].view(torch.int16).numpy().view(np.uint16)
+    want = np.concatenate([x[:, 0::2], x[:, 1::2]], axis=1)
+    assert np.array_equal(g_k.reshape(-1, 64)[case.index.numpy()], want)

@@ -1,0 +1,92 @@
+"""GPU parity of qsa_prepare against the float64 oracle: block keys within
+2**-7*|ref| + 1e-6, untouched block rows bit-exact, carry outputs bit-exact
+(they are copies), device status bits equal; chained calls through the carry
+outputs equal one call."""
+import numpy as np
+import pytest
+import torch
+
+from attention_prologue_kv_gb300 import workloads as wl
+from helpers import compare_cache, run_gpu_qsa, run_oracle_qsa
+
+pytestmark = pytest.mark.gpu
+
+
+def check(case, carry=True):
+    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, carry=carry)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, carry=carry)
+    assert g_st == r_st
+    n, exact = compare_cache(g_bk, r_bk, "bf16", case.Di)
+    if carry:
+        assert np.array_equal(g_nr, r_nr, equal_nan=True)
+        if case.Dr:
+            assert np.array_equal(g_npr, r_npr, equal_nan=True)
+    return n, exact
+
+
+def test_workload_full_size():
+    case = wl.qsa_prepare_workload()
+    n, exact = check(case)
+    assert n == 32 * 32 == case.completed_blocks()
+    assert exact > 0.97
+
+
+@pytest.mark.parametrize("Di,Dr,kbs", [(128, 64, 64), (24, 8, 5), (16, 16, 2), (12, 4, 3),
+                                       (2048, 64, 16), (4096, 128, 4), (4000, 0, 7), (8, 2, 64)])
+def test_shapes(Di, Dr, kbs):
+    case = wl.make_qsa_case("s", 5, 37, Di=Di, Dr=Dr, kbs=kbs, seed=Di + kbs, past_max=300,
+                            rope=Dr > 0)
+    check(case)
+
+
+@pytest.mark.parametrize("rope,norm", [(False, False), (False, True), (True, False)])
+def test_features_disabled(rope, norm):
+    case = wl.make_qsa_case("f", 6, 50, Di=32, Dr=8, kbs=4, seed=7, rope=rope, norm=norm)
+    check(case)
+
+
+def test_shared_key_length():
+    case = wl.make_qsa_case("k", 4, 33, Di=64, Dr=16, kbs=8, seed=8, shared_length=True)
+    check(case)
+
+
+def test_no_block_completed_only_carry():
+    case = wl.make_qsa_case("c", 3, 3, Di=32, Dr=8, kbs=16, seed=9, past=[0, 5, 12])
+    n, _ = check(case)
+    # key lengths 3, 8, 15 with kbs 16: no block completes; only the carry outputs change
+    assert n == case.completed_blocks() == 0
+
+
+def test_device_status_bits():
+    case = wl.make_qsa_case("e", 3, 16, Di=16, Dr=8, kbs=4, seed=10, past=[0, 3, 40], Bcap=12)
+    case.key_length = torch.tensor([10, 19, 56])   # sequence 0: key_length < L; sequence 2: blocks >= Bcap
+    r_bk, _, _, r_st = run_oracle_qsa(case)
+    assert r_st == 0x2 | 0x4
+    check(case)
+
+
+def test_chained_calls_on_gpu_equal_one_call():
+    N, L, Di, Dr, kbs = 4, 45, 32, 8, 6
+    case = wl.make_qsa_case("t", N, L, Di=Di, Dr=Dr, kbs=kbs, seed=11, past=[0, 5, 13, 6], Bcap=12)
+    whole, _, _, _ = run_gpu_qsa(case, carry=False)
+    import attention_prologue_kv_gb300 as kvr
+    dev = "cuda"
+    bk = torch.full((N, 12, Di), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    past_raw, past_rope = case.past_raw.to(dev), case.past_rope.to(dev)
+    P = torch.tensor(case.meta["past"])
+    for a, b in [(0, 7), (7, 30), (30, L)]:
+        nr = torch.full((N, kbs - 1, Di), float("nan"), dtype=torch.bfloat16, device=dev)
+        npr = torch.full((N, 2 * Dr), float("nan"), dtype=torch.bfloat16, device=dev)
+        kvr.qsa_prepare(case.raw[:, a:b].contiguous().to(dev), bk, (P + b).to(dev),
+                        case.rope_cos[:, a:b].contiguous().to(dev), case.rope_sin[:, a:b].contiguous().to(dev),
+                        case.k_norm_weight.to(dev), past_raw, past_rope, kbs, case.eps,
+                        next_incomplete_raw_keys=nr, next_incomplete_rope=npr)
+        past_raw, past_rope = nr, npr
+    torch.cuda.synchronize()
+    assert np.array_equal(bk.cpu().view(torch.int16).numpy(), whole.view(np.int16))
+
+
+def test_empty():
+    case = wl.make_qsa_case("z", 3, 0, Di=32, Dr=8, kbs=4, seed=12)
+    g_bk, _, _, st = run_gpu_qsa(case)
+    assert st == 0 and np.all(g_bk == wl.SENTINEL16)
