@@ -24,50 +24,21 @@
 #include <mutex>
 #include <utility>
 
-#include "kvr_internal.cuh"
+#include "kv_common.cuh"
 
 namespace kvr {
 
-constexpr int KV_THREADS = 128;
-constexpr int KV_WARPS = KV_THREADS / 32;
-constexpr int64_t ROW_SKIP = -1;
-constexpr int64_t ROW_BAD = -2;
-
-// Position in `index` of the entry that governs token t.
-__device__ __forceinline__ int64_t index_pos(const KvParams& p, int64_t t) {
-    if (p.mode == KVR_CACHE_PA_BLK_BSND) {
-        int64_t b = t / p.Skv;
-        int64_t s = t - b * p.Skv;
-        return b * p.nblk + s / p.d1;
-    }
-    return t;
-}
-
-// Flat cache row (in units of one D*-row) for token t with index entry v.
-__device__ __forceinline__ int64_t resolve_row(const KvParams& p, int64_t t, int64_t v) {
-    if (v == -1) return ROW_SKIP;
-    if (p.mode == KVR_CACHE_NORM) {
-        if (v < 0 || v >= p.d1) return ROW_BAD;
-        return (t / p.Skv) * p.d1 + v;
-    }
-    const int64_t nslots = p.d0 * p.d1;
-    if (v < 0 || v >= nslots) return ROW_BAD;
-    if (p.mode == KVR_CACHE_PA_BSND) return v;
-    const int64_t off = (t % p.Skv) % p.d1;
-    if ((v % p.d1) + off >= p.d1) return ROW_BAD;
-    return v + off;
-}
-
+// Registers of one row in flight: the index entry, CPL 16-byte chunks of the
+// Dv part, and this lane's RoPE pair with its four table entries.
 struct RowRegs {
     int64_t v;
     uint4 x[4];
-    uint4 xr;
-    uint2 c0, c1, s0, s1;
+    uint32_t xp;
+    uint16_t c0, c1, s0, s1;
 };
 
 template <int CPL>
-__device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane, int nch, int nrl,
-                                         int h, RowRegs& r) {
+__device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane, int nch, int h, RowRegs& r) {
     r.v = ld_stream_s64(p.index + index_pos(p, t));
     const char* x = static_cast<const char*>(p.kv) + t * p.kv_stride * 2;
 #pragma unroll
@@ -75,144 +46,87 @@ __device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane,
         const int ch = c * 32 + lane;
         if (ch < nch) r.x[c] = ld_stream_v4(x + ch * 16);
     }
-    if (lane < nrl) {
-        r.xr = ld_stream_v4(x + int64_t(p.Dv) * 2 + lane * 16);
-        const char* cr = static_cast<const char*>(p.cos) + t * p.Dk * 2;
-        const char* sr = static_cast<const char*>(p.sin) + t * p.Dk * 2;
-        r.c0 = ld_stream_v2(cr + lane * 8);
-        r.c1 = ld_stream_v2(cr + h * 2 + lane * 8);
-        r.s0 = ld_stream_v2(sr + lane * 8);
-        r.s1 = ld_stream_v2(sr + h * 2 + lane * 8);
+    if (lane < h) {
+        r.xp = ld_stream_u32(x + int64_t(p.Dv) * 2 + lane * 4);
+        const uint16_t* cr = static_cast<const uint16_t*>(p.cos) + t * p.Dk;
+        const uint16_t* sr = static_cast<const uint16_t*>(p.sin) + t * p.Dk;
+        r.c0 = ld_stream_u16(cr + lane);
+        r.c1 = ld_stream_u16(cr + h + lane);
+        r.s0 = ld_stream_u16(sr + lane);
+        r.s1 = ld_stream_u16(sr + h + lane);
     }
 }
 
-// Vector path: Dv % 8 == 0 and Dv <= 256*CPL, Dk % 8 == 0 and Dk <= 256,
-// 16-byte aligned rows. CK = OutKind of the ckv cache.
+// Register path: Dv % 8 == 0 and Dv <= 256*CPL, Dk % 8 == 0, 16-byte aligned
+// rows. Lowest latency for small batches (every load of a row is issued
+// before any of its results is needed; the next row's loads are issued right
+// after the current row's stores). CK = OutKind of the ckv cache.
 template <class IT, int CPL, int CK>
-__global__ void __launch_bounds__(KV_THREADS) kv_vec_kernel(const KvParams p) {
+__global__ void __launch_bounds__(KV_THREADS, 8) kv_vec_kernel(const KvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    uint4* s_gamma = reinterpret_cast<uint4*>(smem);                  // Dv 16-bit values
-    float* s_cscale = reinterpret_cast<float*>(smem + p.Dv * 2);      // Dv floats
-    float* s_kscale = s_cscale + p.Dv;                                // Dk floats
+    const int nch = p.Dv >> 3;
+    float4* g_lo = reinterpret_cast<float4*>(smem);
+    float4* g_hi = g_lo + nch;
+    float4* c_lo = g_hi + nch;
+    float4* c_hi = c_lo + nch;
+    float* s_kscale = reinterpret_cast<float*>(c_hi + nch);
 
     const int lane = threadIdx.x & 31;
-    const int nch = p.Dv >> 3;
-    const int nrl = p.Dk >> 3;
     const int h = p.Dk >> 1;
     const int64_t stride_rows = int64_t(gridDim.x) * KV_WARPS;
     int64_t t = int64_t(blockIdx.x) * KV_WARPS + (threadIdx.x >> 5);
 
+    pdl_wait();
+    pdl_launch_dependents();
     RowRegs r;
-    if (t < p.T) load_row<CPL>(p, t, lane, nch, nrl, h, r);
+    if (t < p.T) load_row<CPL>(p, t, lane, nch, h, r);
 
-    // Stage per-channel constants once per CTA (overlaps the first row's loads).
-    for (int i = threadIdx.x; i < nch; i += KV_THREADS)
-        s_gamma[i] = ld_stream_v4(static_cast<const char*>(p.gamma) + i * 16);
-    const bool cq = CK != OUT16;
+    // Per-channel constants, staged once per CTA while the first row loads.
+    stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, KV_THREADS);
+    const bool cper = CK != OUT16 && p.ckv_scale_per_ch;
     const bool kq = p.k_kind != OUT16;
-    if (cq && p.ckv_scale_per_ch)
-        for (int i = threadIdx.x; i < p.Dv; i += KV_THREADS) s_cscale[i] = p.ckv_scale[i];
+    if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, KV_THREADS);
     if (kq && p.k_scale_per_ch)
         for (int i = threadIdx.x; i < p.Dk; i += KV_THREADS) s_kscale[i] = p.k_scale[i];
-    const float cscale0 = (cq && !p.ckv_scale_per_ch) ? p.ckv_scale[0] : 1.f;
+    const float cscale0 = (CK != OUT16 && !p.ckv_scale_per_ch) ? p.ckv_scale[0] : 1.f;
     const float kscale0 = (kq && !p.k_scale_per_ch) ? p.k_scale[0] : 1.f;
+    const float* kscale = (kq && p.k_scale_per_ch) ? s_kscale : nullptr;
     __syncthreads();
 
     while (t < p.T) {
         const int64_t row = resolve_row(p, t, r.v);
         if (row >= 0) {
-            // ---- RMSNorm of the Dv part ----
-            float ss = 0.f;
+            float2 xg[CPL][4];
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
-                if (c * 32 + lane < nch) {
-                    const uint32_t w[4] = {r.x[c].x, r.x[c].y, r.x[c].z, r.x[c].w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float a = IT::lo(w[k]), b = IT::hi(w[k]);
-                        ss = fmaf(a, a, ss);
-                        ss = fmaf(b, b, ss);
-                    }
-                }
+                const int ch = c * 32 + lane;
+                if (ch < nch) chunk_xg<IT>(r.x[c], g_lo[ch], g_hi[ch], xg[c], acc);
             }
-            ss = warp_sum(ss);
+            const float ss = warp_sum(acc.x + acc.y);
             const float rr = rsqrtf(fmaf(ss, p.inv_dv, p.eps)) * p.alpha;
             char* crow = static_cast<char*>(p.ckv) + row * p.Dv * (CK == OUT16 ? 2 : 1);
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const int ch = c * 32 + lane;
-                if (ch < nch) {
-                    const uint4 gv = s_gamma[ch];
-                    const uint32_t w[4] = {r.x[c].x, r.x[c].y, r.x[c].z, r.x[c].w};
-                    const uint32_t g[4] = {gv.x, gv.y, gv.z, gv.w};
-                    float y[8];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        y[2 * k] = IT::lo(w[k]) * rr * IT::lo(g[k]);
-                        y[2 * k + 1] = IT::hi(w[k]) * rr * IT::hi(g[k]);
-                    }
-                    if constexpr (CK == OUT16) {
-                        uint4 o;
-                        o.x = IT::pack(y[0], y[1]);
-                        o.y = IT::pack(y[2], y[3]);
-                        o.z = IT::pack(y[4], y[5]);
-                        o.w = IT::pack(y[6], y[7]);
-                        *reinterpret_cast<uint4*>(crow + ch * 16) = o;
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            y[k] *= p.ckv_scale_per_ch ? s_cscale[ch * 8 + k] : cscale0;
-                        uint2 o;
-                        o.x = enc8x2<CK>(y[0], y[1]) | (enc8x2<CK>(y[2], y[3]) << 16);
-                        o.y = enc8x2<CK>(y[4], y[5]) | (enc8x2<CK>(y[6], y[7]) << 16);
-                        *reinterpret_cast<uint2*>(crow + ch * 8) = o;
-                    }
-                }
+                if (ch < nch)
+                    chunk_store<IT, CK>(crow + ch * (CK == OUT16 ? 16 : 8), xg[c], rr, cper ? &c_lo[ch] : nullptr,
+                                        cper ? &c_hi[ch] : nullptr, cscale0);
             }
-            // ---- interleaved RoPE of the Dk part: lane owns pairs 4*lane .. 4*lane+3 ----
-            if (lane < nrl) {
-                const uint32_t w[4] = {r.xr.x, r.xr.y, r.xr.z, r.xr.w};
-                const uint32_t cw0[2] = {r.c0.x, r.c0.y}, cw1[2] = {r.c1.x, r.c1.y};
-                const uint32_t sw0[2] = {r.s0.x, r.s0.y}, sw1[2] = {r.s1.x, r.s1.y};
-                float o1[4], o2[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float a = IT::lo(w[k]);   // x1[i] = x[2i]
-                    const float b = IT::hi(w[k]);   // x2[i] = x[2i+1]
-                    const float ca = (k & 1) ? IT::hi(cw0[k >> 1]) : IT::lo(cw0[k >> 1]);
-                    const float sa = (k & 1) ? IT::hi(sw0[k >> 1]) : IT::lo(sw0[k >> 1]);
-                    const float cb = (k & 1) ? IT::hi(cw1[k >> 1]) : IT::lo(cw1[k >> 1]);
-                    const float sb = (k & 1) ? IT::hi(sw1[k >> 1]) : IT::lo(sw1[k >> 1]);
-                    o1[k] = a * ca - b * sa;        // lane i:      x1*cos + (-x2)*sin
-                    o2[k] = b * cb + a * sb;        // lane i+Dk/2: x2*cos + x1*sin
-                }
-                if (p.k_kind == OUT16) {
-                    char* krow = static_cast<char*>(p.kc) + row * p.Dk * 2;
-                    uint2 q1, q2;
-                    q1.x = IT::pack(o1[0], o1[1]);
-                    q1.y = IT::pack(o1[2], o1[3]);
-                    q2.x = IT::pack(o2[0], o2[1]);
-                    q2.y = IT::pack(o2[2], o2[3]);
-                    *reinterpret_cast<uint2*>(krow + lane * 8) = q1;
-                    *reinterpret_cast<uint2*>(krow + h * 2 + lane * 8) = q2;
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        o1[k] *= p.k_scale_per_ch ? s_kscale[lane * 4 + k] : kscale0;
-                        o2[k] *= p.k_scale_per_ch ? s_kscale[h + lane * 4 + k] : kscale0;
-                    }
-                    char* krow = static_cast<char*>(p.kc) + row * p.Dk;
-                    const uint32_t q1 = enc8x2_rt(p.k_kind, o1[0], o1[1]) | (enc8x2_rt(p.k_kind, o1[2], o1[3]) << 16);
-                    const uint32_t q2 = enc8x2_rt(p.k_kind, o2[0], o2[1]) | (enc8x2_rt(p.k_kind, o2[2], o2[3]) << 16);
-                    *reinterpret_cast<uint32_t*>(krow + lane * 4) = q1;
-                    *reinterpret_cast<uint32_t*>(krow + h + lane * 4) = q2;
-                }
+            char* krow = static_cast<char*>(p.kc) + row * p.Dk * (kq ? 1 : 2);
+            if (lane < h) rope_pair_store<IT>(krow, lane, h, r.xp, r.c0, r.s0, r.c1, r.s1, p.k_kind, kscale, kscale0);
+            for (int i = lane + 32; i < h; i += 32) {
+                const char* x = static_cast<const char*>(p.kv) + t * p.kv_stride * 2;
+                const uint16_t* cr = static_cast<const uint16_t*>(p.cos) + t * p.Dk;
+                const uint16_t* sr = static_cast<const uint16_t*>(p.sin) + t * p.Dk;
+                rope_pair_store<IT>(krow, i, h, ld_stream_u32(x + int64_t(p.Dv) * 2 + i * 4), cr[i], sr[i], cr[h + i],
+                                    sr[h + i], p.k_kind, kscale, kscale0);
             }
         } else if (row == ROW_BAD && lane == 0 && p.status != nullptr) {
             atomicOr(p.status, KVR_DEVERR_INDEX);
         }
         t += stride_rows;
-        if (t < p.T) load_row<CPL>(p, t, lane, nch, nrl, h, r);
+        if (t < p.T) load_row<CPL>(p, t, lane, nch, h, r);
     }
 }
 
@@ -225,6 +139,8 @@ __global__ void __launch_bounds__(KV_THREADS) kv_generic_kernel(const KvParams p
     const uint16_t* gamma = static_cast<const uint16_t*>(p.gamma);
     const uint16_t* cosb = static_cast<const uint16_t*>(p.cos);
     const uint16_t* sinb = static_cast<const uint16_t*>(p.sin);
+    pdl_wait();
+    pdl_launch_dependents();
     for (int64_t t = int64_t(blockIdx.x) * KV_WARPS + (threadIdx.x >> 5); t < p.T;
          t += int64_t(gridDim.x) * KV_WARPS) {
         const int64_t row = resolve_row(p, t, p.index[index_pos(p, t)]);
@@ -310,24 +226,23 @@ static int ctas_per_sm(const void* fn, size_t smem) {
     return n;
 }
 
-cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, bool vec, cudaStream_t s) {
+cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, cudaStream_t s) {
+    if (path == KV_BULK) return launch_kv_bulk(p, in_dtype, ckv_kind, s);
     const int64_t rows_ctas = (p.T + KV_WARPS - 1) / KV_WARPS;
     const int sms = sm_count_current_device();
-    if (vec) {
+    if (path == KV_VEC) {
         const int nch = p.Dv / 8;
         const int cpl = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
         VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind) : pick_cpl<F16>(cpl, ckv_kind);
-        const size_t smem = size_t(p.Dv) * 2 + size_t(p.Dv) * 4 + size_t(p.Dk) * 4;
+        const size_t smem = size_t(p.Dv) * 8 + size_t(p.Dk) * 4;
         const int64_t cap = int64_t(ctas_per_sm(reinterpret_cast<const void*>(fn), smem)) * sms;
         const int grid = int(rows_ctas < cap ? rows_ctas : cap);
-        fn<<<grid, KV_THREADS, smem, s>>>(p);
-    } else {
-        auto fn = in_dtype == KVR_BF16 ? kv_generic_kernel<BF16> : kv_generic_kernel<F16>;
-        const int64_t cap = int64_t(ctas_per_sm(reinterpret_cast<const void*>(fn), 0)) * sms;
-        const int grid = int(rows_ctas < cap ? rows_ctas : cap);
-        fn<<<grid, KV_THREADS, 0, s>>>(p, ckv_kind);
+        return launch_pdl(fn, dim3(grid), dim3(KV_THREADS), smem, s, p);
     }
-    return cudaGetLastError();
+    auto fn = in_dtype == KVR_BF16 ? kv_generic_kernel<BF16> : kv_generic_kernel<F16>;
+    const int64_t cap = int64_t(ctas_per_sm(reinterpret_cast<const void*>(fn), 0)) * sms;
+    const int grid = int(rows_ctas < cap ? rows_ctas : cap);
+    return launch_pdl(fn, dim3(grid), dim3(KV_THREADS), size_t(0), s, p, ckv_kind);
 }
 
 }  // namespace kvr

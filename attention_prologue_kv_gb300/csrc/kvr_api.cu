@@ -48,6 +48,12 @@ cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaSt
 
 using namespace kvr;
 
+// Smallest batch (token rows) that takes the bulk-copy pipeline; smaller
+// batches take the register path, whose latency is lower.
+#ifndef KVR_BULK_MIN_ROWS
+#define KVR_BULK_MIN_ROWS 8192
+#endif
+
 namespace {
 
 bool is16(kvr_dtype d) { return d == KVR_BF16 || d == KVR_F16; }
@@ -136,7 +142,7 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
             return KVR_ERR_ALIAS;
     if (overlap(a->ckv_cache, ckv_bytes, a->k_cache, k_bytes)) return KVR_ERR_ALIAS;
 
-    KvParams p;
+    KvParams p = {};
     p.kv = a->kv;
     p.gamma = a->gamma;
     p.cos = a->cos;
@@ -163,12 +169,21 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
     p.inv_dv = 1.0f / float(a->Dv);
     p.alpha = a->kc_scale;
 
+    // Kernel path: the bulk-copy pipeline and the register path need 16-byte
+    // rows (Dv, Dk multiples of 8, 16-byte aligned bases and row stride);
+    // anything else takes the element-wise path.
     const bool ckv8 = is8(a->ckv_dtype), k8 = is8(a->k_dtype);
     const bool vec = (a->Dv % 8 == 0) && a->Dv <= 1024 && (a->Dk % 8 == 0) && a->Dk <= 256 && (stride % 8 == 0) &&
                      aligned(a->kv, 16) && aligned(a->gamma, 16) && aligned(a->cos, 16) && aligned(a->sin, 16) &&
                      aligned(a->ckv_cache, ckv8 ? 8 : 16) && aligned(a->k_cache, k8 ? 4 : 8);
+    int path = vec ? KV_VEC : KV_GENERIC;
+    if (vec && T >= KVR_BULK_MIN_ROWS) {
+        path = KV_BULK;
+        p.kv_contig = stride == D;
+        p.idx_bulk = a->mode != KVR_CACHE_PA_BLK_BSND && aligned(a->index, 16);
+    }
     (void)cudaGetLastError();
-    return cuda_status(launch_kv(p, a->in_dtype, out_kind(a->ckv_dtype), vec, stream));
+    return cuda_status(launch_kv(p, a->in_dtype, out_kind(a->ckv_dtype), path, stream));
 }
 
 kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
@@ -238,8 +253,10 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
     p.inv_kbs = 1.0f / float(kbs);
 
     const bool vec = (a->Di % 8 == 0) && aligned(a->raw_index_keys, 16) && aligned(a->past_incomplete_raw_keys, 16);
+    const bool bulk = vec && (Dr % 8 == 0) && aligned(a->rope_cos, 16) && aligned(a->rope_sin, 16) &&
+                      aligned(a->past_incomplete_rope, 16);
     (void)cudaGetLastError();
-    return cuda_status(launch_qsa(p, a->in_dtype, vec, stream));
+    return cuda_status(launch_qsa(p, a->in_dtype, vec, bulk, stream));
 }
 
 kvr_status kvr_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream) {

@@ -84,11 +84,84 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
     asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
     return r;
 }
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+    uint32_t r;
+    asm("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
+    uint16_t r;
+    asm("ld.global.nc.L1::no_allocate.b16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
 __device__ __forceinline__ int64_t ld_stream_s64(const int64_t* p) {
     int64_t r;
     asm("ld.global.nc.L1::no_allocate.s64 %0, [%1];" : "=l"(r) : "l"(p));
     return r;
 }
+
+// ---------------------------------------------------------------------------
+// mbarrier, bulk async copy (TMA engine), programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Longest any wait in these kernels may take before it gives up, raises
+// KVR_DEVERR_TIMEOUT and lets the CTA drain and exit (a correct run waits
+// for microseconds).
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Make mbarrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait until the phase with parity `parity` of `bar` has completed. Returns
+// false if *abort becomes non-zero (when abort is given) or WAIT_LIMIT_NS passes.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort != nullptr && *abort) return false;
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+// One bulk copy global -> shared, completion counted in bytes on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Programmatic dependent launch: wait for the preceding grid's results (a
+// no-op without the launch attribute), then let the next grid launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -117,6 +190,12 @@ struct KvParams {
     int64_t d0, d1;      // cache leading dims
     int64_t nblk;        // PA_BLK_BSND: index entries per sequence
     int Dv, Dk;
+    // bulk (TMA) pipeline layout, set by the host for the pipelined kernel
+    int R;               // rows per tile
+    int S;               // pipeline stages
+    int kv_contig;       // kv rows are dense: one bulk copy per tile
+    int idx_bulk;        // the index tile is bulk-copied (else read from global)
+    uint32_t stage_bytes, off_cos, off_sin, off_idx, off_consts, off_stages;
     int mode;            // kvr_cache_mode
     int k_kind;          // OutKind of the k cache
     int ckv_scale_per_ch, k_scale_per_ch;
@@ -142,9 +221,31 @@ struct QsaParams {
     float eps, inv_di, inv_kbs;
 };
 
+// Launch with programmatic stream serialisation allowed: the grid may be
+// scheduled while the previous kernel on the stream drains; its kernels call
+// pdl_wait() before touching global memory.
+template <typename... Args>
+cudaError_t launch_pdl(void (*fn)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
+// Kernel paths of the KV prologue, chosen by the host from shapes and alignment.
+enum KvPath : int { KV_GENERIC = 0, KV_VEC = 1, KV_BULK = 2 };
+
 // Launchers (host), defined next to their kernels. Return a CUDA error code.
-cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, bool vec, cudaStream_t s);
-cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, cudaStream_t s);
+cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, cudaStream_t s);
+cudaError_t launch_kv_bulk(const KvParams& p, int in_dtype, int ckv_kind, cudaStream_t s);
+cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, cudaStream_t s);
 cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s);
 
 int sm_count_current_device();

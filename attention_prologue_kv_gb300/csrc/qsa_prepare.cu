@@ -18,6 +18,9 @@
 // the block-wide sum of squares, the rotation and one rounding to the
 // output type follow; the 2*Di-byte key row is written once. One extra CTA
 // per sequence writes the optional carry outputs.
+#include <mutex>
+#include <set>
+
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -61,6 +64,8 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
     const int64_t n = int64_t(blockIdx.x) / per_seq;
     const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
 
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t K = p.key_length[p.key_length_per_seq ? n : 0];
     const int64_t P = K - p.L;
     if (P < 0) {
@@ -185,19 +190,213 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
     }
 }
 
-cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, cudaStream_t s) {
+// ---------------------------------------------------------------------------
+// Bulk-copy variant: the block's kbs rows (carried rows, then new rows: each
+// run contiguous) and its first token's cos/sin arrive in shared memory by
+// one to four bulk copies, so every block's bytes are requested at once and
+// the whole problem is one wave of loads. Needs Di % 8 == 0, Dr % 8 == 0,
+// 16-byte aligned bases and kbs*Di*2 bytes of shared memory.
+// ---------------------------------------------------------------------------
+
+constexpr int QSA_BULK_THREADS = 128;
+
+template <class IT>
+__global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    const int Di = p.Di;
+    const int64_t kbs = p.kbs;
+    unsigned char* rows_s = smem + 128;                                      // kbs x Di 16-bit
+    uint16_t* rope_s = reinterpret_cast<uint16_t*>(rows_s + kbs * Di * 2);   // [cos | sin] of the first token
+    const int C = Di / 8;
+    const int G = C >= QSA_BULK_THREADS ? 1 : QSA_BULK_THREADS / C;
+    float* part = reinterpret_cast<float*>(rope_s + 2 * p.Dr + 8);          // [G][Di]
+    float* u = part + G * Di;                                                // [Di]
+    float* red = u + Di;                                                     // [QSA_BULK_THREADS/32 + 1]
+    const int tid = threadIdx.x;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int64_t per_seq = p.nbmax + 1;
+    const int64_t n = int64_t(blockIdx.x) / per_seq;
+    const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
+    const int64_t K = p.key_length[p.key_length_per_seq ? n : 0];
+    const int64_t P = K - p.L;
+    if (P < 0) {
+        if (jl == 0 && tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_KEY_LENGTH);
+        return;
+    }
+    const int64_t F = P - P % kbs;
+    const int64_t j0 = P / kbs;
+    const int64_t nb = K / kbs - j0;
+    const uint16_t* raw = static_cast<const uint16_t*>(p.raw) + n * p.L * Di;
+    const uint16_t* past = static_cast<const uint16_t*>(p.past_raw) + n * (kbs - 1) * Di;
+
+    if (jl == p.nbmax) {
+        // carry outputs (small; plain loads and stores)
+        const int64_t Fn = (K / kbs) * kbs;
+        const int64_t rem = K - Fn;
+        if (p.next_raw != nullptr) {
+            uint16_t* dst = static_cast<uint16_t*>(p.next_raw) + n * (kbs - 1) * Di;
+            for (int64_t e = tid; e < rem * Di; e += QSA_BULK_THREADS) {
+                const int64_t r = e / Di, ch = e - r * Di;
+                const int64_t tok = Fn + r;
+                dst[e] = tok < P ? past[(tok - F) * Di + ch] : raw[(tok - P) * Di + ch];
+            }
+        }
+        if (p.next_rope != nullptr && p.Dr > 0 && rem > 0) {
+            uint16_t* dst = static_cast<uint16_t*>(p.next_rope) + n * 2 * p.Dr;
+            for (int e = tid; e < 2 * p.Dr; e += QSA_BULK_THREADS) {
+                uint16_t v;
+                if (Fn >= P) {
+                    const int64_t row = (n * p.L + (Fn - P)) * p.Dr;
+                    v = e < p.Dr ? static_cast<const uint16_t*>(p.cos)[row + e]
+                                 : static_cast<const uint16_t*>(p.sin)[row + e - p.Dr];
+                } else {
+                    v = static_cast<const uint16_t*>(p.past_rope)[n * 2 * p.Dr + e];
+                }
+                dst[e] = v;
+            }
+        }
+        return;
+    }
+    if (jl >= nb) return;
+    const int64_t j = j0 + jl;
+    if (j >= p.Bcap) {
+        if (tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_BLOCK_CAP);
+        return;
+    }
+    const int64_t tok0 = j * kbs;
+    const int64_t n_past = tok0 < P ? P - tok0 : 0;   // only the first block can hold carried rows
+    const int64_t n_new = kbs - n_past;
+    const uint32_t row_b = uint32_t(Di) * 2;
+
+    if (tid == 0) {
+        const uint32_t rope_b = uint32_t(p.Dr) * 2;
+        mbar_arrive_expect_tx(bar, uint32_t(kbs) * row_b + 2 * rope_b);
+        if (n_past > 0) bulk_g2s(rows_s, past + (tok0 - F) * Di, uint32_t(n_past) * row_b, bar);
+        bulk_g2s(rows_s + n_past * row_b, raw + (tok0 + n_past - P) * Di, uint32_t(n_new) * row_b, bar);
+        if (p.Dr > 0) {
+            if (tok0 >= P) {
+                const int64_t row = (n * p.L + (tok0 - P)) * p.Dr;
+                bulk_g2s(rope_s, static_cast<const uint16_t*>(p.cos) + row, rope_b, bar);
+                bulk_g2s(rope_s + p.Dr, static_cast<const uint16_t*>(p.sin) + row, rope_b, bar);
+            } else {
+                bulk_g2s(rope_s, static_cast<const uint16_t*>(p.past_rope) + n * 2 * p.Dr, 2 * rope_b, bar);
+            }
+        }
+    }
+    if (!mbar_wait(bar, 0, nullptr)) {
+        if (tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_TIMEOUT);
+        mbar_wait(bar, 0, nullptr);   // the copies must land before the CTA exits
+        return;
+    }
+
+    // ---- block sum from shared memory: thread (g, c) sums rows g, g+G, ... of chunk c ----
+    for (int cbase = 0; cbase < (C > QSA_BULK_THREADS ? C : 1); cbase += QSA_BULK_THREADS) {
+        const int c = C >= QSA_BULK_THREADS ? cbase + tid : tid % C;
+        const int g = C >= QSA_BULK_THREADS ? 0 : tid / C;
+        if (c < C && g < G) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int64_t r = g; r < kbs; r += G) {
+                const uint4 v = *reinterpret_cast<const uint4*>(rows_s + r * row_b + c * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc[2 * k] += IT::lo(w[k]);
+                    acc[2 * k + 1] += IT::hi(w[k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) part[g * Di + c * 8 + k] = acc[k];
+        }
+    }
+    __syncthreads();
+
+    // ---- mean, optional RMS normalisation ----
+    float ss = 0.f;
+    for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) {
+        float s = 0.f;
+        for (int g = 0; g < G; ++g) s += part[g * Di + ch];
+        const float m = s / float(kbs);
+        u[ch] = m;
+        ss = fmaf(m, m, ss);
+    }
+    if (p.w != nullptr) {
+        float v = warp_sum(ss);
+        if ((tid & 31) == 0) red[tid >> 5] = v;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < QSA_BULK_THREADS / 32; ++w) tot += red[w];
+        const float rr = rsqrtf(fmaf(tot, p.inv_di, p.eps));
+        const uint16_t* wt = static_cast<const uint16_t*>(p.w);
+        for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) u[ch] = u[ch] * rr * IT::one(wt[ch]);
+    }
+    __syncthreads();
+
+    // ---- rotation of the last Dr channels, one rounding, write the key row ----
+    const int base = Di - p.Dr;
+    const int h = p.Dr >> 1;
+    uint16_t* out = static_cast<uint16_t*>(p.block_keys) + (n * p.Bcap + j) * Di;
+    for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) {
+        float v;
+        if (ch < base) {
+            v = u[ch];
+        } else {
+            const int i = ch - base;
+            const int q = i < h ? i : i - h;
+            const float a = u[base + 2 * q];
+            const float b = u[base + 2 * q + 1];
+            const float c = IT::one(rope_s[i]);
+            const float s = IT::one(rope_s[p.Dr + i]);
+            v = i < h ? a * c - b * s : b * c + a * s;
+        }
+        out[ch] = IT::one_out(v);
+    }
+}
+
+// Shared memory the bulk variant needs (0 if it does not fit).
+static size_t qsa_bulk_smem(const QsaParams& p) {
+    const int C = p.Di / 8;
+    const int G = C >= QSA_BULK_THREADS ? 1 : QSA_BULK_THREADS / C;
+    const size_t bytes = 128 + size_t(p.kbs) * p.Di * 2 + (2 * size_t(p.Dr) + 8) * 2 +
+                         (size_t(G) * p.Di + p.Di + QSA_BULK_THREADS / 32 + 1) * 4;
+    return bytes <= 96 * 1024 ? bytes : 0;
+}
+
+cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, cudaStream_t s) {
+    const int64_t grid = p.N * (p.nbmax + 1);
+    const size_t bsmem = bulk ? qsa_bulk_smem(p) : 0;
+    if (bsmem > 0) {
+        auto fn = in_dtype == KVR_BF16 ? qsa_bulk_kernel<BF16> : qsa_bulk_kernel<F16>;
+        if (bsmem > 48 * 1024) {
+            static std::mutex mu;
+            static std::set<const void*> done;
+            std::lock_guard<std::mutex> lock(mu);
+            if (!done.count(reinterpret_cast<const void*>(fn))) {
+                cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+                if (e != cudaSuccess) return e;
+                done.insert(reinterpret_cast<const void*>(fn));
+            }
+        }
+        return launch_pdl(fn, dim3(unsigned(grid)), dim3(QSA_BULK_THREADS), bsmem, s, p);
+    }
     const int C = vec ? p.Di / 8 : p.Di;
     const int G = C >= QSA_THREADS ? 1 : QSA_THREADS / C;
     const size_t smem = (size_t(G) * p.Di + p.Di + QSA_THREADS / 32 + 1) * sizeof(float);
-    const int64_t grid = p.N * (p.nbmax + 1);
     if (vec) {
         auto fn = in_dtype == KVR_BF16 ? qsa_kernel<BF16, 8> : qsa_kernel<F16, 8>;
-        fn<<<unsigned(grid), QSA_THREADS, smem, s>>>(p);
-    } else {
-        auto fn = in_dtype == KVR_BF16 ? qsa_kernel<BF16, 1> : qsa_kernel<F16, 1>;
-        fn<<<unsigned(grid), QSA_THREADS, smem, s>>>(p);
+        return launch_pdl(fn, dim3(unsigned(grid)), dim3(QSA_THREADS), smem, s, p);
     }
-    return cudaGetLastError();
+    auto fn = in_dtype == KVR_BF16 ? qsa_kernel<BF16, 1> : qsa_kernel<F16, 1>;
+    return launch_pdl(fn, dim3(unsigned(grid)), dim3(QSA_THREADS), smem, s, p);
 }
 
 }  // namespace kvr

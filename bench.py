@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--only", choices=["prefill_paged", "quant_fp8", "tiny_norm", "qsa_prepare", "decode_paged"],
+                    help="run W + K launches of one workload and print their timing (for profilers)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -442,14 +444,36 @@ def e2e_decode(args, sets, gamma, ckv, kc, dev, kvr):
             "how": "public Python API, one packed pinned H2D copy + call + status D2H per step, one stream"}
 
 
+def time_graph(calls, n_calls, stream):
+    """Average duration of one call when n_calls calls (cycling through
+    `calls`) run back to back as one CUDA graph replay."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_calls):
+            calls[i % len(calls)]()
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / n_calls
+
+
 def run_extras(dev, kvr, wl, flush_buf):
-    """The other workloads, each timed per launch with L2 flushed before it."""
+    """The other workloads. Each is timed two ways: isolated (one launch after
+    an L2 flush, event-timed, launch latency included) and steady (back-to-back
+    launches in a CUDA graph over input sets that together exceed L2)."""
     import torch
     out = {}
     stream = torch.cuda.current_stream()
     flush = lambda: l2_flush(flush_buf)
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs", 6800.0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
     # in-process copy reference (16-byte vectorised device copy, 2 x 512 MB)
     src = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -459,49 +483,65 @@ def run_extras(dev, kvr, wl, flush_buf):
     out["copy_peak_gbs_in_run"] = copy_gbs
     del src, dst
 
-    def kv_case(case):
-        D = case.Dv + case.Dk
-        kv = case.kv.to(dev)
-        ckv = torch.zeros(case.cache_shapes()[0], dtype=wl.code_torch_dtype(case.ckv_dtype), device=dev).view(
-            wl.TORCH_DTYPES[case.ckv_dtype])
-        kc = torch.zeros(case.cache_shapes()[1], dtype=wl.code_torch_dtype(case.k_dtype), device=dev).view(
-            wl.TORCH_DTYPES[case.k_dtype])
-        args = (kv, case.gamma.to(dev), case.cos.to(dev), case.sin.to(dev), case.index.to(dev), ckv, kc)
-        kw = dict(cache_mode=case.mode, eps=case.eps,
-                  ckv_scale=None if case.ckv_scale is None else case.ckv_scale.to(dev))
-        fn = lambda: kvr.kv_rmsnorm_rope_cache(*args, **kw)
-        for _ in range(3):
-            fn()
-        med, best = time_each(fn, 20, flush, stream)
-        act = case.active_tokens()
-        nbytes = kv_algorithmic_bytes(act, case.T - act, case.Dv, case.Dk,
-                                      ckv_bytes=1 if case.ckv_dtype != "bf16" else 2,
-                                      scale_bytes=0 if case.ckv_scale is None else 4 * case.ckv_scale.numel())
-        gbs = nbytes / (med / 1e3) / 1e9
-        return {"tokens": case.T, "us_median": med * 1e3, "us_min": best * 1e3,
-                "tokens_per_s": case.T / (med / 1e3), "bytes": nbytes, "gbs": gbs,
+    def summary(us_iso, us_steady, nbytes, units, unit_name):
+        gbs = nbytes / (us_steady / 1e6) / 1e9
+        return {unit_name: units, "bytes": nbytes, "us_isolated": us_iso, "us_steady": us_steady,
+                unit_name + "_per_s": units / (us_steady / 1e6), "gbs": gbs,
                 "frac_of_measured_peak": gbs / peak, "frac_of_copy_in_run": gbs / copy_gbs,
-                "frac_of_nominal_8000": gbs / 8000.0}
+                "frac_of_nominal_8000": gbs / 8000.0,
+                "gbs_isolated": nbytes / (us_iso / 1e6) / 1e9}
 
-    out["prefill_paged"] = kv_case(wl.prefill_paged())
-    out["quant_fp8"] = kv_case(wl.quant_fp8())
-    out["tiny_norm"] = kv_case(wl.tiny_norm())
+    def kv_workload(make, seeds):
+        cases = [make(seed=s) for s in seeds]
+        c0 = cases[0]
+        ckv = torch.zeros(c0.cache_shapes()[0], dtype=wl.code_torch_dtype(c0.ckv_dtype), device=dev).view(
+            wl.TORCH_DTYPES[c0.ckv_dtype])
+        kc = torch.zeros(c0.cache_shapes()[1], dtype=wl.code_torch_dtype(c0.k_dtype), device=dev).view(
+            wl.TORCH_DTYPES[c0.k_dtype])
+        calls = []
+        for c in cases:
+            a = (c.kv.to(dev), c.gamma.to(dev), c.cos.to(dev), c.sin.to(dev), c.index.to(dev), ckv, kc)
+            kw = dict(cache_mode=c.mode, eps=c.eps, ckv_scale=None if c.ckv_scale is None else c.ckv_scale.to(dev))
+            calls.append(lambda a=a, kw=kw: kvr.kv_rmsnorm_rope_cache(*a, **kw))
+        for f in calls:
+            f()
+        iso, _ = time_each(calls[0], 20, flush, stream)
+        steady = time_graph(calls, 8 * len(calls), stream)
+        act = c0.active_tokens()
+        nbytes = kv_algorithmic_bytes(act, c0.T - act, c0.Dv, c0.Dk,
+                                      ckv_bytes=1 if c0.ckv_dtype != "bf16" else 2,
+                                      scale_bytes=0 if c0.ckv_scale is None else 4 * c0.ckv_scale.numel())
+        in_set = c0.T * ((c0.Dv + c0.Dk) * 2 + 4 * c0.Dk + 8)
+        r = summary(iso * 1e3, steady * 1e3, nbytes, c0.T, "tokens")
+        r["sets"] = "%d input sets x %.1f MB" % (len(cases), in_set / 1e6)
+        return r
 
-    q = wl.qsa_prepare_workload()
-    bk = torch.zeros(q.N, q.Bcap, q.Di, dtype=torch.bfloat16, device=dev)
+    def nsets(bytes_per_set):
+        return max(3, int(2 * l2 // bytes_per_set) + 1)
+
+    out["prefill_paged"] = kv_workload(wl.prefill_paged, [1003 + 7919 * i for i in range(3)])
+    out["quant_fp8"] = kv_workload(wl.quant_fp8, [1004 + 7919 * i for i in range(nsets(4096 * 1416))])
+    out["tiny_norm"] = kv_workload(wl.tiny_norm, [1001])
+
+    qs = [wl.qsa_prepare_workload(seed=1005 + 7919 * i) for i in range(nsets(17.3e6))]
+    q0 = qs[0]
+    bk = torch.zeros(q0.N, q0.Bcap, q0.Di, dtype=torch.bfloat16, device=dev)
     d = lambda t: t.to(dev)
-    qargs = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
+    calls = []
+    for q in qs:
+        a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
              d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
-    fn = lambda: kvr.qsa_prepare(*qargs)
-    for _ in range(3):
-        fn()
-    med, best = time_each(fn, 20, flush, stream)
-    nb = q.completed_blocks()
-    nbytes = qsa_algorithmic_bytes(nb, q.N, q.kbs, q.Di, q.Dr)
-    gbs = nbytes / (med / 1e3) / 1e9
-    out["qsa_prepare"] = {"new_tokens": q.N * q.L, "blocks": nb, "us_median": med * 1e3, "us_min": best * 1e3,
-                          "new_tokens_per_s": q.N * q.L / (med / 1e3), "bytes": nbytes, "gbs": gbs,
-                          "frac_of_measured_peak": gbs / peak, "frac_of_copy_in_run": gbs / copy_gbs}
+        calls.append(lambda a=a: kvr.qsa_prepare(*a))
+    for f in calls:
+        f()
+    iso, _ = time_each(calls[0], 20, flush, stream)
+    steady = time_graph(calls, 8 * len(calls), stream)
+    nb = q0.completed_blocks()
+    r = summary(iso * 1e3, steady * 1e3, qsa_algorithmic_bytes(nb, q0.N, q0.kbs, q0.Di, q0.Dr),
+                q0.N * q0.L, "new_tokens")
+    r["blocks"] = nb
+    r["sets"] = "%d input sets" % len(qs)
+    out["qsa_prepare"] = r
     torch.cuda.synchronize()
     return out
 
@@ -552,9 +592,56 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_only(args):
+    """W + K launches of a single workload, timed per launch (no L2 flush, no
+    graphs): a small, self-contained command for profilers."""
+    import torch
+
+    import attention_prologue_kv_gb300 as kvr
+    from attention_prologue_kv_gb300 import workloads as wl
+    from attention_prologue_kv_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    if args.only == "qsa_prepare":
+        q = wl.qsa_prepare_workload()
+        bk = torch.zeros(q.N, q.Bcap, q.Di, dtype=torch.bfloat16, device=dev)
+        d = lambda t: t.to(dev)
+        a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
+             d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
+        fn = lambda: kvr.qsa_prepare(*a)
+    else:
+        case = getattr(wl, args.only)()
+        ckv = torch.zeros(case.cache_shapes()[0], dtype=wl.code_torch_dtype(case.ckv_dtype), device=dev).view(
+            wl.TORCH_DTYPES[case.ckv_dtype])
+        kc = torch.zeros(case.cache_shapes()[1], dtype=wl.code_torch_dtype(case.k_dtype), device=dev).view(
+            wl.TORCH_DTYPES[case.k_dtype])
+        a = (case.kv.to(dev), case.gamma.to(dev), case.cos.to(dev), case.sin.to(dev), case.index.to(dev), ckv, kc)
+        kw = dict(cache_mode=case.mode, eps=case.eps,
+                  ckv_scale=None if case.ckv_scale is None else case.ckv_scale.to(dev))
+        fn = lambda: kvr.kv_rmsnorm_rope_cache(*a, **kw)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return {"only": args.only, "launches": args.warmup + args.steps, "us_median": statistics.median(ts),
+            "us_min": min(ts)}
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, _ = dist_env()
+    if args.only:
+        print(json.dumps(run_only(args)), flush=True)
+        return 0
     if args.impl == "reference":
         if rank != 0:
             return 0

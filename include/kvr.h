@@ -33,7 +33,12 @@
  *   - Data-dependent errors are found on the device: the offending row or
  *     block is skipped (never written out of bounds) and, if `dev_status`
  *     is non-NULL, the matching KVR_DEVERR_* bit is OR-ed into *dev_status.
- *     No kernel traps, asserts or spins.
+ *     No kernel traps or asserts. Waits inside a kernel (its copy pipeline)
+ *     are bounded: past one second a kernel raises KVR_DEVERR_TIMEOUT, lets
+ *     its copies in flight land, and returns.
+ *   - Each launch uses programmatic dependent launch: it may start while the
+ *     previous kernel on the stream finishes, and waits for that kernel's
+ *     results before it reads any input.
  *   - An empty problem (T = Bkv*Skv = 0, or N*L = 0) returns KVR_OK with no
  *     launch, mirroring the empty-tensor rule of "aclnnMlaPrologV3WeightNz"
  *     ("Shape restrictions": caches are not updated).
@@ -68,6 +73,8 @@ typedef enum kvr_status {
 #define KVR_DEVERR_INDEX 0x1       /* kv: an index entry outside {-1} U [0, range) */
 #define KVR_DEVERR_KEY_LENGTH 0x2  /* qsa: key_length[n] < L (the past length would be negative) */
 #define KVR_DEVERR_BLOCK_CAP 0x4   /* qsa: a completed block's number is >= Bcap */
+#define KVR_DEVERR_TIMEOUT 0x8     /* a pipeline wait inside a kernel exceeded its limit
+                                      (one second); that CTA stopped early, output incomplete */
 
 typedef enum kvr_dtype {
     KVR_BF16 = 0,

@@ -114,7 +114,7 @@ def test_out_of_range_indices_are_skipped_and_flagged():
     ref_ckv, ref_k, ref_st = run_oracle_kv(case)
     assert ref_st == 1
     n, _, _ = check(case)
-    assert n == 32 - 3
+    assert n == case.T - 3   # T = 4 x 32 = 128 tokens fill the 128 slots; 3 are bad
 
 
 def test_all_skipped_and_empty():
