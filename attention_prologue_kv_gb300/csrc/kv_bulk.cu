@@ -33,7 +33,10 @@
 
 namespace kvr {
 
-constexpr int BULK_CONSUMERS = 16;
+#ifndef KVR_BULK_CONSUMERS
+#define KVR_BULK_CONSUMERS 16
+#endif
+constexpr int BULK_CONSUMERS = KVR_BULK_CONSUMERS;
 constexpr int BULK_THREADS = 32 * (1 + BULK_CONSUMERS);
 
 template <class IT, int CPL, int CK>

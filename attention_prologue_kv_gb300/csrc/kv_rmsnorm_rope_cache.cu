@@ -26,6 +26,11 @@
 
 #include "kv_common.cuh"
 
+// Batches below this many rows (16-bit caches) keep gamma in registers.
+#ifndef KVR_REG_GAMMA_MAX_ROWS
+#define KVR_REG_GAMMA_MAX_ROWS 2048
+#endif
+
 namespace kvr {
 
 // Registers of one row in flight: the index entry, CPL 16-byte chunks of the
@@ -58,11 +63,19 @@ __device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane,
 }
 
 // Register path: Dv % 8 == 0 and Dv <= 256*CPL, Dk % 8 == 0, 16-byte aligned
-// rows. Lowest latency for small batches (every load of a row is issued
-// before any of its results is needed; the next row's loads are issued right
-// after the current row's stores). CK = OutKind of the ckv cache.
-template <class IT, int CPL, int CK>
-__global__ void __launch_bounds__(KV_THREADS, 8) kv_vec_kernel(const KvParams p) {
+// rows. Every load of a row is issued before any of its results is needed,
+// and the next row's loads are issued right after the current row's stores.
+// CK = OutKind of ckv. Two flavours for the per-channel constants:
+//  * REG_GAMMA (16-bit caches, small batches): gamma lives in registers for
+//    the whole kernel; no shared memory and no CTA barrier, so the first row
+//    starts as soon as its loads land (lowest latency);
+//  * otherwise gamma and the scales are staged once per CTA in shared
+//    memory, pre-widened to float (fewest instructions per row).
+#ifndef KVR_VEC_MIN_CTAS
+#define KVR_VEC_MIN_CTAS 8
+#endif
+template <class IT, int CPL, int CK, bool REG_GAMMA>
+__global__ void __launch_bounds__(KV_THREADS, REG_GAMMA ? 6 : KVR_VEC_MIN_CTAS) kv_vec_kernel(const KvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int nch = p.Dv >> 3;
     float4* g_lo = reinterpret_cast<float4*>(smem);
@@ -78,20 +91,31 @@ __global__ void __launch_bounds__(KV_THREADS, 8) kv_vec_kernel(const KvParams p)
 
     pdl_wait();
     pdl_launch_dependents();
+    if (REG_GAMMA && t >= p.T) return;
     RowRegs r;
     if (t < p.T) load_row<CPL>(p, t, lane, nch, h, r);
 
-    // Per-channel constants, staged once per CTA while the first row loads.
-    stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, KV_THREADS);
     const bool cper = CK != OUT16 && p.ckv_scale_per_ch;
     const bool kq = p.k_kind != OUT16;
-    if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, KV_THREADS);
-    if (kq && p.k_scale_per_ch)
-        for (int i = threadIdx.x; i < p.Dk; i += KV_THREADS) s_kscale[i] = p.k_scale[i];
     const float cscale0 = (CK != OUT16 && !p.ckv_scale_per_ch) ? p.ckv_scale[0] : 1.f;
     const float kscale0 = (kq && !p.k_scale_per_ch) ? p.k_scale[0] : 1.f;
-    const float* kscale = (kq && p.k_scale_per_ch) ? s_kscale : nullptr;
-    __syncthreads();
+    const float* kscale = nullptr;
+    uint4 graw[CPL];
+    if constexpr (REG_GAMMA) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int ch = c * 32 + lane;
+            if (ch < nch) graw[c] = ld_stream_v4(static_cast<const char*>(p.gamma) + ch * 16);
+        }
+        kscale = (kq && p.k_scale_per_ch) ? p.k_scale : nullptr;
+    } else {
+        stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, KV_THREADS);
+        if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, KV_THREADS);
+        if (kq && p.k_scale_per_ch)
+            for (int i = threadIdx.x; i < p.Dk; i += KV_THREADS) s_kscale[i] = p.k_scale[i];
+        kscale = (kq && p.k_scale_per_ch) ? s_kscale : nullptr;
+        __syncthreads();
+    }
 
     while (t < p.T) {
         const int64_t row = resolve_row(p, t, r.v);
@@ -101,7 +125,15 @@ __global__ void __launch_bounds__(KV_THREADS, 8) kv_vec_kernel(const KvParams p)
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const int ch = c * 32 + lane;
-                if (ch < nch) chunk_xg<IT>(r.x[c], g_lo[ch], g_hi[ch], xg[c], acc);
+                if (ch < nch) {
+                    if constexpr (REG_GAMMA) {
+                        const uint4 g = graw[c];
+                        chunk_xg<IT>(r.x[c], make_float4(IT::lo(g.x), IT::hi(g.x), IT::lo(g.y), IT::hi(g.y)),
+                                     make_float4(IT::lo(g.z), IT::hi(g.z), IT::lo(g.w), IT::hi(g.w)), xg[c], acc);
+                    } else {
+                        chunk_xg<IT>(r.x[c], g_lo[ch], g_hi[ch], xg[c], acc);
+                    }
+                }
             }
             const float ss = warp_sum(acc.x + acc.y);
             const float rr = rsqrtf(fmaf(ss, p.inv_dv, p.eps)) * p.alpha;
@@ -192,20 +224,20 @@ __global__ void __launch_bounds__(KV_THREADS) kv_generic_kernel(const KvParams p
 typedef void (*VecKernel)(const KvParams);
 
 template <class IT, int CPL>
-static VecKernel pick_ck(int ck) {
+static VecKernel pick_ck(int ck, bool reg_gamma) {
     switch (ck) {
-        case OUT16: return kv_vec_kernel<IT, CPL, OUT16>;
-        case OUT_I8: return kv_vec_kernel<IT, CPL, OUT_I8>;
-        case OUT_E4M3: return kv_vec_kernel<IT, CPL, OUT_E4M3>;
-        default: return kv_vec_kernel<IT, CPL, OUT_E5M2>;
+        case OUT16: return reg_gamma ? kv_vec_kernel<IT, CPL, OUT16, true> : kv_vec_kernel<IT, CPL, OUT16, false>;
+        case OUT_I8: return kv_vec_kernel<IT, CPL, OUT_I8, false>;
+        case OUT_E4M3: return kv_vec_kernel<IT, CPL, OUT_E4M3, false>;
+        default: return kv_vec_kernel<IT, CPL, OUT_E5M2, false>;
     }
 }
 
 template <class IT>
-static VecKernel pick_cpl(int cpl, int ck) {
-    if (cpl == 1) return pick_ck<IT, 1>(ck);
-    if (cpl == 2) return pick_ck<IT, 2>(ck);
-    return pick_ck<IT, 4>(ck);
+static VecKernel pick_cpl(int cpl, int ck, bool reg_gamma) {
+    if (cpl == 1) return pick_ck<IT, 1>(ck, reg_gamma);
+    if (cpl == 2) return pick_ck<IT, 2>(ck, reg_gamma);
+    return pick_ck<IT, 4>(ck, reg_gamma);
 }
 
 // Resident CTAs per SM for (kernel, dynamic shared memory), computed once and
@@ -233,8 +265,12 @@ cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, c
     if (path == KV_VEC) {
         const int nch = p.Dv / 8;
         const int cpl = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
-        VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind) : pick_cpl<F16>(cpl, ckv_kind);
-        const size_t smem = size_t(p.Dv) * 8 + size_t(p.Dk) * 4;
+        // Register-held gamma for small batches into 16-bit caches (latency),
+        // shared-memory constants otherwise (instructions per row).
+        const bool reg_gamma = ckv_kind == OUT16 && p.T < KVR_REG_GAMMA_MAX_ROWS;
+        VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind, reg_gamma)
+                                            : pick_cpl<F16>(cpl, ckv_kind, reg_gamma);
+        const size_t smem = reg_gamma ? 0 : size_t(p.Dv) * 8 + size_t(p.Dk) * 4;
         const int64_t cap = int64_t(ctas_per_sm(reinterpret_cast<const void*>(fn), smem)) * sms;
         const int grid = int(rows_ctas < cap ? rows_ctas : cap);
         return launch_pdl(fn, dim3(grid), dim3(KV_THREADS), smem, s, p);

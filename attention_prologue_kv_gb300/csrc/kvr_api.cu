@@ -175,7 +175,8 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
     const bool ckv8 = is8(a->ckv_dtype), k8 = is8(a->k_dtype);
     const bool vec = (a->Dv % 8 == 0) && a->Dv <= 1024 && (a->Dk % 8 == 0) && a->Dk <= 256 && (stride % 8 == 0) &&
                      aligned(a->kv, 16) && aligned(a->gamma, 16) && aligned(a->cos, 16) && aligned(a->sin, 16) &&
-                     aligned(a->ckv_cache, ckv8 ? 8 : 16) && aligned(a->k_cache, k8 ? 4 : 8);
+                     aligned(a->ckv_cache, ckv8 ? 8 : 16) && aligned(a->k_cache, k8 ? 4 : 8) &&
+                     aligned(a->ckv_scale, 16);
     int path = vec ? KV_VEC : KV_GENERIC;
     if (vec && T >= KVR_BULK_MIN_ROWS) {
         path = KV_BULK;
@@ -254,7 +255,7 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
 
     const bool vec = (a->Di % 8 == 0) && aligned(a->raw_index_keys, 16) && aligned(a->past_incomplete_raw_keys, 16);
     const bool bulk = vec && (Dr % 8 == 0) && aligned(a->rope_cos, 16) && aligned(a->rope_sin, 16) &&
-                      aligned(a->past_incomplete_rope, 16);
+                      aligned(a->past_incomplete_rope, 16) && aligned(a->k_norm_weight, 16);
     (void)cudaGetLastError();
     return cuda_status(launch_qsa(p, a->in_dtype, vec, bulk, stream));
 }

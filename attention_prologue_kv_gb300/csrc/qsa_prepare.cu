@@ -193,9 +193,10 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 // ---------------------------------------------------------------------------
 // Bulk-copy variant: the block's kbs rows (carried rows, then new rows: each
 // run contiguous) and its first token's cos/sin arrive in shared memory by
-// one to four bulk copies, so every block's bytes are requested at once and
-// the whole problem is one wave of loads. Needs Di % 8 == 0, Dr % 8 == 0,
-// 16-byte aligned bases and kbs*Di*2 bytes of shared memory.
+// a few bulk copies (with k_norm_weight), so every block's bytes are
+// requested at once and the whole problem is one wave of loads. Needs
+// Di % 8 == 0, Dr % 8 == 0, 16-byte aligned bases and about kbs*Di*2 bytes
+// of shared memory.
 // ---------------------------------------------------------------------------
 
 constexpr int QSA_BULK_THREADS = 128;
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     const int Di = p.Di;
     const int64_t kbs = p.kbs;
     unsigned char* rows_s = smem + 128;                                      // kbs x Di 16-bit
-    uint16_t* rope_s = reinterpret_cast<uint16_t*>(rows_s + kbs * Di * 2);   // [cos | sin] of the first token
+    uint16_t* w_s = reinterpret_cast<uint16_t*>(rows_s + kbs * Di * 2);      // k_norm_weight [Di]
+    uint16_t* rope_s = w_s + Di;                                             // [cos | sin] of the first token
     const int C = Di / 8;
     const int G = C >= QSA_BULK_THREADS ? 1 : QSA_BULK_THREADS / C;
     float* part = reinterpret_cast<float*>(rope_s + 2 * p.Dr + 8);          // [G][Di]
@@ -279,7 +281,9 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
 
     if (tid == 0) {
         const uint32_t rope_b = uint32_t(p.Dr) * 2;
-        mbar_arrive_expect_tx(bar, uint32_t(kbs) * row_b + 2 * rope_b);
+        const uint32_t w_b = p.w != nullptr ? row_b : 0;
+        mbar_arrive_expect_tx(bar, uint32_t(kbs) * row_b + 2 * rope_b + w_b);
+        if (w_b) bulk_g2s(w_s, p.w, w_b, bar);
         if (n_past > 0) bulk_g2s(rows_s, past + (tok0 - F) * Di, uint32_t(n_past) * row_b, bar);
         bulk_g2s(rows_s + n_past * row_b, raw + (tok0 + n_past - P) * Di, uint32_t(n_new) * row_b, bar);
         if (p.Dr > 0) {
@@ -292,11 +296,19 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
             }
         }
     }
-    if (!mbar_wait(bar, 0, nullptr)) {
-        if (tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_TIMEOUT);
-        mbar_wait(bar, 0, nullptr);   // the copies must land before the CTA exits
-        return;
+    // Thread 0 waits for the copies; the rest of the CTA sleeps in the barrier
+    // (which also orders thread 0's observation before every thread's reads).
+    __shared__ int timed_out;
+    if (tid == 0) {
+        timed_out = 0;
+        if (!mbar_wait(bar, 0, nullptr)) {
+            timed_out = 1;
+            if (p.status != nullptr) atomicOr(p.status, KVR_DEVERR_TIMEOUT);
+            mbar_wait(bar, 0, nullptr);   // the copies must land before the CTA exits
+        }
     }
+    __syncthreads();
+    if (timed_out) return;
 
     // ---- block sum from shared memory: thread (g, c) sums rows g, g+G, ... of chunk c ----
     for (int cbase = 0; cbase < (C > QSA_BULK_THREADS ? C : 1); cbase += QSA_BULK_THREADS) {
@@ -336,8 +348,7 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
 #pragma unroll
         for (int w = 0; w < QSA_BULK_THREADS / 32; ++w) tot += red[w];
         const float rr = rsqrtf(fmaf(tot, p.inv_di, p.eps));
-        const uint16_t* wt = static_cast<const uint16_t*>(p.w);
-        for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) u[ch] = u[ch] * rr * IT::one(wt[ch]);
+        for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) u[ch] = u[ch] * rr * IT::one(w_s[ch]);
     }
     __syncthreads();
 
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
 static size_t qsa_bulk_smem(const QsaParams& p) {
     const int C = p.Di / 8;
     const int G = C >= QSA_BULK_THREADS ? 1 : QSA_BULK_THREADS / C;
-    const size_t bytes = 128 + size_t(p.kbs) * p.Di * 2 + (2 * size_t(p.Dr) + 8) * 2 +
+    const size_t bytes = 128 + size_t(p.kbs) * p.Di * 2 + size_t(p.Di) * 2 + (2 * size_t(p.Dr) + 8) * 2 +
                          (size_t(G) * p.Di + p.Di + QSA_BULK_THREADS / 32 + 1) * 4;
     return bytes <= 96 * 1024 ? bytes : 0;
 }

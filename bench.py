@@ -55,6 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--extras-only", action="store_true", help="time only the other workloads")
     ap.add_argument("--only", choices=["prefill_paged", "quant_fp8", "tiny_norm", "qsa_prepare", "decode_paged"],
                     help="run W + K launches of one workload and print their timing (for profilers)")
     a = ap.parse_args(argv)
@@ -482,6 +483,17 @@ def run_extras(dev, kvr, wl, flush_buf):
     copy_gbs = 2 * src.numel() / (best / 1e3) / 1e9
     out["copy_peak_gbs_in_run"] = copy_gbs
     del src, dst
+    # the same copy at the prefill's size (42 MB read + 42 MB written per call),
+    # back to back over rotating sources: what a plain copy reaches at this size
+    half = 84149248 // 2 // 16 * 16
+    n_pairs = int(2 * l2 // (2 * half)) + 2
+    bufs = [(torch.empty(half, dtype=torch.uint8, device=dev), torch.empty(half, dtype=torch.uint8, device=dev))
+            for _ in range(n_pairs)]
+    calls = [lambda b=b: kvr.device_copy(b[1], b[0]) for b in bufs]
+    us = time_graph(calls, 8 * len(calls), stream) * 1e3
+    out["copy_84MB_steady"] = {"us": us, "gbs": 2 * half / (us / 1e6) / 1e9,
+                               "how": "%d (src, dst) pairs of %.0f MB rotated" % (n_pairs, half / 1e6)}
+    del bufs
 
     def summary(us_iso, us_steady, nbytes, units, unit_name):
         gbs = nbytes / (us_steady / 1e6) / 1e9
@@ -646,6 +658,18 @@ def main(argv=None):
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if args.extras_only:
+        import torch
+
+        import attention_prologue_kv_gb300 as kvr
+        from attention_prologue_kv_gb300 import workloads as wl
+        from attention_prologue_kv_gb300.build import build
+        build()
+        dev = torch.device("cuda", 0)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+        print(json.dumps({"extras": run_extras(dev, kvr, wl, flush_buf)}), flush=True)
         return 0
     res = run_ours(args)
     if res is not None:
