@@ -43,7 +43,7 @@ WORKLOAD = ("decode_paged: Bkv=256 Skv=1 N=1 D=576 (Dv=512 rmsnorm, Dk=64 interl
             "BlockSize=128 BlockNum=4096, 256 distinct slots per batch with 5 (2%) set to -1")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kv_rmsnorm_rope_cache__decode_paged.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "attention_prologue_kv_gb300", "csrc", f)
-                  for f in ("kv_rmsnorm_rope_cache.cu", "kvr_internal.cuh")]
+                  for f in ("kv_rmsnorm_rope_cache.cu", "kv_common.cuh", "kvr_internal.cuh")]
 
 
 def parse_args(argv=None):
