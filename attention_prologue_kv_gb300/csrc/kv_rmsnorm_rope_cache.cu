@@ -89,6 +89,14 @@ __global__ void __launch_bounds__(KV_THREADS, REG_GAMMA ? 6 : KVR_VEC_MIN_CTAS) 
     const int64_t stride_rows = int64_t(gridDim.x) * KV_WARPS;
     int64_t t = int64_t(blockIdx.x) * KV_WARPS + (threadIdx.x >> 5);
 
+    // While the preceding grid may still run, start this warp's first row on
+    // its way from HBM into L2 (see prefetch_l2_bulk).
+    if (t < p.T && lane == 0) {
+        prefetch_l2_bulk(static_cast<const char*>(p.kv) + t * p.kv_stride * 2, uint32_t(p.Dv + p.Dk) * 2);
+        prefetch_l2_bulk(static_cast<const char*>(p.cos) + t * p.Dk * 2, uint32_t(p.Dk) * 2);
+        prefetch_l2_bulk(static_cast<const char*>(p.sin) + t * p.Dk * 2, uint32_t(p.Dk) * 2);
+        prefetch_l2(p.index + index_pos(p, t));
+    }
     pdl_wait();
     pdl_launch_dependents();
     if (REG_GAMMA && t >= p.T) return;

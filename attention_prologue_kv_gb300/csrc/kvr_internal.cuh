@@ -160,6 +160,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// L2 prefetch hints. They move nothing into registers or shared memory and
+// L2 is the point of coherence, so they may run before pdl_wait(): a write
+// by the preceding grid to a prefetched line still lands in L2 and is what
+// the later loads see. Bulk form: 16-byte aligned address, size a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // Programmatic dependent launch: wait for the preceding grid's results (a
 // no-op without the launch attribute), then let the next grid launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     float* red = u + Di;                                                     // [QSA_BULK_THREADS/32 + 1]
     const int tid = threadIdx.x;
 
+    const int64_t per_seq = p.nbmax + 1;
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
@@ -225,7 +226,6 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     pdl_wait();
     pdl_launch_dependents();
 
-    const int64_t per_seq = p.nbmax + 1;
     const int64_t n = int64_t(blockIdx.x) / per_seq;
     const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
     const int64_t K = p.key_length[p.key_length_per_seq ? n : 0];
