@@ -52,8 +52,16 @@ class QsaArgs(ctypes.Structure):
     ]
 
 
-EXPORTS = ("kv_rmsnorm_rope_cache", "qsa_prepare", "kvr_device_copy", "kvr_status_string",
-           "kvr_abi_version")
+class DqArgs(ctypes.Structure):
+    _fields_ = [
+        ("q_nope", _vp), ("in_dtype", _int),
+        ("rows", _i64), ("Hckv", _i64), ("q_row_stride", _i64),
+        ("q_out", _vp), ("dequant_scale", _vp),
+    ]
+
+
+EXPORTS = ("kv_rmsnorm_rope_cache", "qsa_prepare", "dynamic_quant", "kvr_device_copy",
+           "kvr_status_string", "kvr_abi_version")
 
 _lib = None
 
@@ -74,6 +82,8 @@ def lib():
     L.kv_rmsnorm_rope_cache.restype = _int
     L.qsa_prepare.argtypes = [ctypes.POINTER(QsaArgs), _vp]
     L.qsa_prepare.restype = _int
+    L.dynamic_quant.argtypes = [ctypes.POINTER(DqArgs), _vp]
+    L.dynamic_quant.restype = _int
     L.kvr_device_copy.argtypes = [_vp, _vp, _i64, _vp]
     L.kvr_device_copy.restype = _int
     L.kvr_status_string.argtypes = [_int]

@@ -183,6 +183,36 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
         raise KvrError(st, "qsa_prepare")
 
 
+def dynamic_quant(q_nope, q_out, dequant_scale, *, stream=None):
+    """DynamicQuant of q^N: per row (last axis, e.g. q^N [T, N, Hckv] gives
+    T*N rows) dequant_scale = RowMax(|q|)/127 and q_out = round(q/scale) as
+    int8. q_nope bf16/f16 with a dense last axis and uniformly strided rows;
+    q_out int8 of q_nope's shape (dense); dequant_scale float32 with one
+    element per row (e.g. [T, N, 1])."""
+    _cuda(q_nope, "q_nope")
+    if q_nope.dtype not in _IN_DTYPES:
+        raise ValueError("q_nope must be bfloat16 or float16")
+    if q_nope.stride(-1) != 1:
+        raise ValueError("q_nope must be dense along its last dimension")
+    H = q_nope.shape[-1]
+    rows = q_nope.numel() // H if H else 0
+    try:
+        q2 = q_nope.view(-1, H)   # never a silent copy: the kernel runs asynchronously
+    except RuntimeError:
+        raise ValueError("q_nope rows must be uniformly strided")
+    stride = q2.stride(0) if rows > 1 else H
+    if q_out.dtype != torch.int8 or q_out.numel() != q_nope.numel():
+        raise ValueError("q_out must be int8 with q_nope's number of elements")
+    if dequant_scale.dtype != torch.float32 or dequant_scale.numel() != rows:
+        raise ValueError("dequant_scale must be float32 with one element per row")
+    a = N.DqArgs(q_nope=q2.data_ptr(), in_dtype=_IN_DTYPES[q_nope.dtype], rows=rows, Hckv=H,
+                 q_row_stride=stride, q_out=_ptr(q_out, "q_out"),
+                 dequant_scale=_ptr(dequant_scale, "dequant_scale"))
+    st = N.lib().dynamic_quant(ctypes.byref(a), _stream(stream))
+    if st != N.KVR_OK:
+        raise KvrError(st, "dynamic_quant")
+
+
 def device_copy(dst, src, stream=None):
     """16-byte vectorised device copy of src into dst (same byte size); the
     in-process HBM bandwidth reference."""

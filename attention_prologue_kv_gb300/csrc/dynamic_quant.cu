@@ -1,0 +1,190 @@
+// DynamicQuant of q^N: per-row symmetric int8 quantisation.
+//
+// Operation: "aclnnMlaPrologV3WeightNz" (hiascend.com), "Formula":
+// dequantScaleQNope = RowMax(abs(q^N)) / 127, q^N = round(q^N / dequantScaleQNope),
+// one scale per (token, head) row ("Shape restrictions": (T, N, 1)).
+//
+// Design: one warp per row, grid-stride, 4 warps per CTA. A lane loads its
+// 16-byte chunks of the row; the row max of |q| is a packed 16-bit maximum
+// and a warp butterfly (exact); the scale is one IEEE division; each code is
+// the IEEE quotient rounded to nearest even (the float32 operations the
+// formula names), obtained from a reciprocal product except near rounding
+// boundaries (dq_code_fast); each lane stores 8 codes with one 8-byte store. The first row of each warp is
+// prefetched into L2 before the programmatic-dependent-launch wait.
+#include <map>
+#include <mutex>
+
+#include "kvr_internal.cuh"
+
+namespace kvr {
+
+constexpr int DQ_THREADS = 128;
+constexpr int DQ_WARPS = DQ_THREADS / 32;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ int dq_code(float x, float s) {
+    if (!(s > 0.f)) return 0;
+    const int c = __float2int_rn(__fdiv_rn(x, s));
+    return min(max(c, -127), 127);
+}
+
+// The same code without a division per element. With y = RN(1/s), the
+// product q0 = RN(x*y) differs from x/s by at most (2^-24 + 2^-24 + 2^-48)|x/s|
+// and from fl32(x/s) by less than 3 ulps of q0, i.e. by less than 2^-16 for
+// |q0| < 128 (codes are at most 127 in magnitude, ulp(q0) <= 2^-17 there).
+// Rounding q0 or fl32(x/s) to an integer can therefore differ only when q0
+// lies within that distance of a half-integer; those elements (rare) take the
+// IEEE division. Valid while 1/s is a normal float: the caller checks
+// s >= 2^-100 for the row.
+__device__ __forceinline__ int dq_code_fast(float x, float s, float y) {
+    const float q0 = x * y;
+    const float r0 = rintf(q0);
+    if (fabsf(fabsf(q0 - r0) - 0.5f) > 0x1p-15f) return min(max(int(r0), -127), 127);
+    return dq_code(x, s);
+}
+
+// max(|a|, |b|) over the two 16-bit lanes of w, exact: clear the sign bits and
+// take the packed bf16/f16 maximum.
+template <class IT>
+__device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w);
+template <>
+__device__ __forceinline__ uint32_t absmax2<BF16>(uint32_t acc, uint32_t w) {
+    w &= 0x7FFF7FFFu;
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&acc), b = *reinterpret_cast<__nv_bfloat162*>(&w);
+    __nv_bfloat162 m = __hmax2(a, b);
+    return *reinterpret_cast<uint32_t*>(&m);
+}
+template <>
+__device__ __forceinline__ uint32_t absmax2<F16>(uint32_t acc, uint32_t w) {
+    w &= 0x7FFF7FFFu;
+    __half2 a = *reinterpret_cast<__half2*>(&acc), b = *reinterpret_cast<__half2*>(&w);
+    __half2 m = __hmax2(a, b);
+    return *reinterpret_cast<uint32_t*>(&m);
+}
+
+// Vector path: H % 8 == 0, H <= 256 * CPL, 16-byte aligned rows and outputs
+// 8-byte aligned. Rows are double-buffered in registers: the loads of a
+// warp's next row are issued before the current row is quantised, so every
+// warp keeps two rows (2 KB for H = 512) in flight.
+template <class IT, int CPL>
+__global__ void __launch_bounds__(DQ_THREADS) dq_vec_kernel(const DqParams p) {
+    const int lane = threadIdx.x & 31;
+    const int nch = int(p.H >> 3);
+    const int64_t stride_rows = int64_t(gridDim.x) * DQ_WARPS;
+    int64_t t = int64_t(blockIdx.x) * DQ_WARPS + (threadIdx.x >> 5);
+    if (t < p.rows && lane == 0)
+        prefetch_l2_bulk(static_cast<const char*>(p.q) + t * p.q_stride * 2, uint32_t(p.H) * 2);
+    pdl_wait();
+    pdl_launch_dependents();
+    uint4 x[CPL], nx[CPL];
+    auto load = [&](int64_t row, uint4 (&dst)[CPL]) {
+        const char* src = static_cast<const char*>(p.q) + row * p.q_stride * 2;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int ch = c * 32 + lane;
+            if (ch < nch) dst[c] = ld_stream_v4(src + ch * 16);
+        }
+    };
+    if (t < p.rows) load(t, x);
+    for (; t < p.rows; t += stride_rows) {
+        if (t + stride_rows < p.rows) load(t + stride_rows, nx);
+        uint32_t am = 0;   // packed |q| maxima
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            if (c * 32 + lane < nch) {
+                am = absmax2<IT>(am, x[c].x);
+                am = absmax2<IT>(am, x[c].y);
+                am = absmax2<IT>(am, x[c].z);
+                am = absmax2<IT>(am, x[c].w);
+            }
+        }
+        const float m = warp_max(fmaxf(IT::lo(am), IT::hi(am)));
+        const float s = __fdiv_rn(m, 127.f);
+        const bool fast = s >= 0x1p-100f;
+        const float y = fast ? __frcp_rn(s) : 0.f;
+        char* dst = reinterpret_cast<char*>(p.out) + t * p.H;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int ch = c * 32 + lane;
+            if (ch < nch) {
+                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+                uint32_t b[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float lo = IT::lo(w[k]), hi = IT::hi(w[k]);
+                    b[2 * k] = uint32_t(fast ? dq_code_fast(lo, s, y) : dq_code(lo, s)) & 0xFFu;
+                    b[2 * k + 1] = uint32_t(fast ? dq_code_fast(hi, s, y) : dq_code(hi, s)) & 0xFFu;
+                }
+                uint2 o;
+                o.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+                o.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+                *reinterpret_cast<uint2*>(dst + ch * 8) = o;
+            }
+        }
+        if (lane == 0) p.scale[t] = s;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) x[c] = nx[c];
+    }
+}
+
+// Generic path: any H, element-aligned rows; two passes over the row.
+template <class IT>
+__global__ void __launch_bounds__(DQ_THREADS) dq_generic_kernel(const DqParams p) {
+    const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t t = int64_t(blockIdx.x) * DQ_WARPS + (threadIdx.x >> 5); t < p.rows;
+         t += int64_t(gridDim.x) * DQ_WARPS) {
+        const uint16_t* src = static_cast<const uint16_t*>(p.q) + t * p.q_stride;
+        float m = 0.f;
+        for (int64_t c = lane; c < p.H; c += 32) m = fmaxf(m, fabsf(IT::one(src[c])));
+        m = warp_max(m);
+        const float s = __fdiv_rn(m, 127.f);
+        int8_t* dst = p.out + t * p.H;
+        for (int64_t c = lane; c < p.H; c += 32) dst[c] = int8_t(dq_code(IT::one(src[c]), s));
+        if (lane == 0) p.scale[t] = s;
+    }
+}
+
+// Resident CTAs per SM of a kernel, queried once per kernel and cached.
+static int dq_ctas_per_sm(const void* fn) {
+    static std::mutex mu;
+    static std::map<const void*, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(fn);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, DQ_THREADS, 0) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    cache[fn] = n;
+    return n;
+}
+
+cudaError_t launch_dq(const DqParams& p, int in_dtype, bool vec, cudaStream_t s) {
+    const int64_t ctas = (p.rows + DQ_WARPS - 1) / DQ_WARPS;
+    const int sms = sm_count_current_device();
+    if (vec) {
+        const int nch = int(p.H / 8);
+        const int cpl = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
+        typedef void (*K)(const DqParams);
+        K fn;
+        if (in_dtype == KVR_BF16)
+            fn = cpl == 1 ? dq_vec_kernel<BF16, 1> : (cpl == 2 ? dq_vec_kernel<BF16, 2> : dq_vec_kernel<BF16, 4>);
+        else
+            fn = cpl == 1 ? dq_vec_kernel<F16, 1> : (cpl == 2 ? dq_vec_kernel<F16, 2> : dq_vec_kernel<F16, 4>);
+        const int64_t cap = int64_t(dq_ctas_per_sm(reinterpret_cast<const void*>(fn))) * sms;
+        return launch_pdl(fn, dim3(int(ctas < cap ? ctas : cap)), dim3(DQ_THREADS), size_t(0), s, p);
+    }
+    auto fn = in_dtype == KVR_BF16 ? dq_generic_kernel<BF16> : dq_generic_kernel<F16>;
+    const int64_t cap = int64_t(dq_ctas_per_sm(reinterpret_cast<const void*>(fn))) * sms;
+    return launch_pdl(fn, dim3(int(ctas < cap ? ctas : cap)), dim3(DQ_THREADS), size_t(0), s, p);
+}
+
+}  // namespace kvr

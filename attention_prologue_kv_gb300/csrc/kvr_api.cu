@@ -260,6 +260,32 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
     return cuda_status(launch_qsa(p, a->in_dtype, vec, bulk, stream));
 }
 
+kvr_status dynamic_quant(const kvr_dq_args* a, cudaStream_t stream) {
+    if (a == nullptr) return KVR_ERR_NULL;
+    if (!is16(a->in_dtype)) return KVR_ERR_DTYPE;
+    const int64_t stride = a->q_row_stride == 0 ? a->Hckv : a->q_row_stride;
+    if (a->rows < 0 || a->Hckv < 1 || stride < a->Hckv) return KVR_ERR_SHAPE;
+    if (a->rows == 0) return KVR_OK;
+    if (a->q_nope == nullptr || a->q_out == nullptr || a->dequant_scale == nullptr) return KVR_ERR_NULL;
+    if (!aligned(a->q_nope, 2) || !aligned(a->dequant_scale, 4)) return KVR_ERR_SHAPE;
+    const int64_t in_bytes = ((a->rows - 1) * stride + a->Hckv) * 2;
+    if (overlap(a->q_out, a->rows * a->Hckv, a->q_nope, in_bytes) ||
+        overlap(a->dequant_scale, a->rows * 4, a->q_nope, in_bytes) ||
+        overlap(a->dequant_scale, a->rows * 4, a->q_out, a->rows * a->Hckv))
+        return KVR_ERR_ALIAS;
+    DqParams p;
+    p.q = a->q_nope;
+    p.out = a->q_out;
+    p.scale = a->dequant_scale;
+    p.rows = a->rows;
+    p.H = a->Hckv;
+    p.q_stride = stride;
+    const bool vec = a->Hckv % 8 == 0 && a->Hckv <= 1024 && stride % 8 == 0 && aligned(a->q_nope, 16) &&
+                     aligned(a->q_out, 8);
+    (void)cudaGetLastError();
+    return cuda_status(launch_dq(p, a->in_dtype, vec, stream));
+}
+
 kvr_status kvr_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream) {
     if (bytes == 0) return KVR_OK;
     if (dst == nullptr || src == nullptr) return KVR_ERR_NULL;

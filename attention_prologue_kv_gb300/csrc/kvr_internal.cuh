@@ -232,6 +232,13 @@ struct QsaParams {
     float eps, inv_di, inv_kbs;
 };
 
+struct DqParams {
+    const void* q;
+    int8_t* out;
+    float* scale;
+    int64_t rows, H, q_stride;
+};
+
 // Launch with programmatic stream serialisation allowed: the grid may be
 // scheduled while the previous kernel on the stream drains; its kernels call
 // pdl_wait() before touching global memory.
@@ -258,6 +265,7 @@ cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, c
 cudaError_t launch_kv_bulk(const KvParams& p, int in_dtype, int ckv_kind, cudaStream_t s);
 cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, cudaStream_t s);
 cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s);
+cudaError_t launch_dq(const DqParams& p, int in_dtype, bool vec, cudaStream_t s);
 
 int sm_count_current_device();
 

@@ -259,6 +259,14 @@ def qsa_prepare_workload(seed=1005):
                          past_max=8192, Bcap=160)
 
 
+def dynamic_quant_decode(seed=1006, T=256, heads=128, Hckv=512, dtype="bf16", row_pad=0):
+    """q^N of one decode step: T tokens x `heads` heads x Hckv, ~N(0, 1), as
+    [T, heads, Hckv] (a column slice of wider rows when row_pad > 0)."""
+    g = torch.Generator().manual_seed(seed)
+    wide = torch.randn(T, heads, Hckv + row_pad, generator=g, dtype=torch.float32).to(TORCH_DTYPES[dtype])
+    return wide[..., :Hckv]
+
+
 KV_WORKLOADS = {
     "tiny_norm": tiny_norm,
     "decode_paged": decode_paged,

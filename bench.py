@@ -75,6 +75,11 @@ def kv_algorithmic_bytes(n_active, n_skipped, Dv=512, Dk=64, in_bytes=2, ckv_byt
     return n_active * per_active + n_skipped * 8 + Dv * in_bytes + scale_bytes
 
 
+def dq_algorithmic_bytes(rows, H, in_bytes=2):
+    """DynamicQuant: read the row, write its int8 codes and one float32 scale."""
+    return rows * (H * in_bytes + H + 4)
+
+
 def qsa_algorithmic_bytes(n_blocks, n_seq, kbs, Di, Dr, in_bytes=2):
     per_block = kbs * Di * in_bytes + 2 * Dr * in_bytes + Di * in_bytes
     return n_blocks * per_block + n_seq * 8 + Di * in_bytes
@@ -554,6 +559,20 @@ def run_extras(dev, kvr, wl, flush_buf):
     r["blocks"] = nb
     r["sets"] = "%d input sets" % len(qs)
     out["qsa_prepare"] = r
+
+    # DynamicQuant of q^N for one decode step (256 tokens x 128 heads x 512)
+    qs = [wl.dynamic_quant_decode(seed=1006 + 7919 * i) for i in range(nsets(256 * 128 * 512 * 2))]
+    rows, H = qs[0].numel() // qs[0].shape[-1], qs[0].shape[-1]
+    outs = [(q.to(dev), torch.empty(q.shape, dtype=torch.int8, device=dev),
+             torch.empty(q.shape[:-1] + (1,), dtype=torch.float32, device=dev)) for q in qs]
+    calls = [lambda o=o: kvr.dynamic_quant(*o) for o in outs]
+    for f in calls:
+        f()
+    iso, _ = time_each(calls[0], 20, flush, stream)
+    steady = time_graph(calls, 8 * len(calls), stream)
+    r = summary(iso * 1e3, steady * 1e3, dq_algorithmic_bytes(rows, H), rows, "rows")
+    r["sets"] = "%d input sets" % len(qs)
+    out["dynamic_quant_decode"] = r
     torch.cuda.synchronize()
     return out
 

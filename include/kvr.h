@@ -1,7 +1,7 @@
 /*
  * kvr.h - C ABI of libkvr.so, the GB300 (sm_103a) attention-prologue key path.
  *
- * Two operations:
+ * Three operations:
  *
  *   kv_rmsnorm_rope_cache()  the fused KV prologue of the page
  *       "aclnnKvRmsNormRopeCache" (hiascend.com, CANN ops-transformer):
@@ -21,6 +21,9 @@
  *       tokens = mean of the block's raw index keys, RMS-normalised with
  *       k_norm_weight, rotated with the RoPE of the block's first token;
  *       incomplete blocks are carried across calls.
+ *
+ *   dynamic_quant()  DynamicQuant of q^N, the query-side step beside this
+ *       path on "aclnnMlaPrologV3WeightNz": per-row int8 codes and scales.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
@@ -213,6 +216,34 @@ typedef struct kvr_qsa_args {
 } kvr_qsa_args;
 
 kvr_status qsa_prepare(const kvr_qsa_args* args, cudaStream_t stream);
+
+/*
+ * Arguments of dynamic_quant(): DynamicQuant of q^N from "aclnnMlaPrologV3WeightNz"
+ * ("Formula": dequantScaleQNope = RowMax(abs(q^N)) / 127,
+ * q^N = round(q^N / dequantScaleQNope); "Shape restrictions": one scale per
+ * (token, head), shape (T, N, 1)).
+ *
+ *   q_nope          [rows, Hckv] input, `in_dtype` (bf16 or f16); rows = T*N
+ *                   (tokens x heads). Row r starts q_row_stride elements after
+ *                   row r-1 (0 means Hckv).
+ *   q_out           [rows, Hckv] int8 codes, dense.
+ *   dequant_scale   [rows] float32 scales.
+ *
+ * Per row: scale = RowMax(|q|) / 127 and code = round-half-even(q / scale),
+ * both float32 IEEE divisions, clamped to [-127, 127]; an all-zero row gets
+ * scale 0 and codes 0. Inputs are finite. Limits: rows >= 0, Hckv >= 1; the
+ * outputs must not overlap the input (KVR_ERR_ALIAS).
+ */
+typedef struct kvr_dq_args {
+    const void* q_nope;
+    kvr_dtype in_dtype;
+    int64_t rows, Hckv;
+    int64_t q_row_stride;
+    int8_t* q_out;
+    float* dequant_scale;
+} kvr_dq_args;
+
+kvr_status dynamic_quant(const kvr_dq_args* args, cudaStream_t stream);
 
 /* Measurement helper (no counterpart on the pages): a 16-byte vectorised
  * device-to-device copy of `bytes` bytes (a multiple of 16, both pointers

@@ -11,6 +11,7 @@ Modules:
   encoders               float64 -> cache codes (bf16, f16, int8, FP8 E4M3FN, FP8 E5M2)
   kv_rmsnorm_rope_cache  RMSNorm + interleaved RoPE + quantise + scatter
   qsa_prepare            QSA block-key prepare with carry across calls
+  dynamic_quant          DynamicQuant of q^N: per-row RowMax/127 scale, int8 codes
 
 Every function is pinned by `-m "not gpu"` tests to closed forms, invariants,
 hand-worked toys (tests/golden) or library routines; no part is
@@ -22,9 +23,11 @@ from .kv_rmsnorm_rope_cache import (NORM, PA_BLK_BSND, PA_BSND, STATUS_INDEX,
                                     ref_kv_rmsnorm_rope_cache,
                                     ref_kv_rmsnorm_rope_cache_loop, rms_norm)
 from .qsa_prepare import STATUS_BLOCK_CAP, STATUS_KEY_LENGTH, ref_qsa_prepare
+from .dynamic_quant import ref_dynamic_quant
 
 __all__ = [
     "encoders", "NORM", "PA_BSND", "PA_BLK_BSND", "STATUS_INDEX", "STATUS_KEY_LENGTH",
     "STATUS_BLOCK_CAP", "cache_slot", "interleave_rope", "quantise", "rms_norm",
     "ref_kv_rmsnorm_rope_cache", "ref_kv_rmsnorm_rope_cache_loop", "ref_qsa_prepare",
+    "ref_dynamic_quant",
 ]

@@ -53,6 +53,7 @@ PROBE = r"""
 int main(void) {
     printf("kvr_kv_args %zu\n", sizeof(kvr_kv_args));
     printf("kvr_qsa_args %zu\n", sizeof(kvr_qsa_args));
+    printf("kvr_dq_args %zu\n", sizeof(kvr_dq_args));
     %FIELDS%
     return 0;
 }
@@ -62,7 +63,7 @@ int main(void) {
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="no C compiler")
 def test_struct_layout_matches_c(tmp_path):
     fields = []
-    for T, cls in (("kvr_kv_args", N.KvArgs), ("kvr_qsa_args", N.QsaArgs)):
+    for T, cls in (("kvr_kv_args", N.KvArgs), ("kvr_qsa_args", N.QsaArgs), ("kvr_dq_args", N.DqArgs)):
         for name, _ in cls._fields_:
             fields.append("F(%s, %s)" % (T, name))
     src = tmp_path / "probe.c"
@@ -75,7 +76,8 @@ def test_struct_layout_matches_c(tmp_path):
     got = dict(line.split() for line in out if line.strip())
     assert int(got["kvr_kv_args"]) == ctypes.sizeof(N.KvArgs)
     assert int(got["kvr_qsa_args"]) == ctypes.sizeof(N.QsaArgs)
-    for T, cls in (("kvr_kv_args", N.KvArgs), ("kvr_qsa_args", N.QsaArgs)):
+    assert int(got["kvr_dq_args"]) == ctypes.sizeof(N.DqArgs)
+    for T, cls in (("kvr_kv_args", N.KvArgs), ("kvr_qsa_args", N.QsaArgs), ("kvr_dq_args", N.DqArgs)):
         for name, _ in cls._fields_:
             assert int(got["%s.%s" % (T, name)]) == getattr(cls, name).offset, (T, name)
 
@@ -164,6 +166,24 @@ def test_qsa_host_validation(lib, kw, want):
 def test_qsa_empty_problem_is_ok(lib):
     assert lib.qsa_prepare(ctypes.byref(_qsa_args(L=0)), None) == N.KVR_OK
     assert lib.qsa_prepare(ctypes.byref(_qsa_args(N=0, key_length_len=0)), None) in (N.KVR_OK, N.KVR_ERR_SHAPE)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(in_dtype=N.KVR_INT8), N.KVR_ERR_DTYPE),
+    (dict(Hckv=0), N.KVR_ERR_SHAPE),
+    (dict(rows=-1), N.KVR_ERR_SHAPE),
+    (dict(q_row_stride=100), N.KVR_ERR_SHAPE),
+    (dict(q_nope=None), N.KVR_ERR_NULL),
+    (dict(dequant_scale=None), N.KVR_ERR_NULL),
+    (dict(q_out=(1 << 20) + 512), N.KVR_ERR_ALIAS),
+    (dict(dequant_scale=(1 << 20) * 4 + 1000), N.KVR_ERR_ALIAS),
+    (dict(rows=0, q_nope=None), N.KVR_OK),
+])
+def test_dynamic_quant_host_validation(lib, kw, want):
+    a = dict(q_nope=1 << 20, in_dtype=N.KVR_BF16, rows=64, Hckv=512, q_row_stride=0,
+             q_out=(1 << 20) * 4, dequant_scale=(1 << 20) * 8)
+    a.update(kw)
+    assert lib.dynamic_quant(ctypes.byref(N.DqArgs(**a)), None) == want
 
 
 def test_device_copy_validation(lib):
