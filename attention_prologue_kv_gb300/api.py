@@ -84,17 +84,8 @@ def _cache_dims(c, name):
     return c.shape[0], c.shape[1], c.shape[-1]
 
 
-def kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
-                          cache_mode="PA_BSND", eps=1e-6, ckv_scale=None, k_scale=None,
-                          kc_scale=1.0, dev_status=None, stream=None):
-    """Fused RMSNorm(kv[..., :Dv]) -> ckv_cache and interleaved RoPE(kv[..., Dv:]) ->
-    k_cache, scattered by `index` (-1 skips). Dv = gamma.numel().
-
-    kv [Bkv, 1, Skv, D] (bf16/f16; rows may be strided, e.g. a column slice),
-    cos/sin [Bkv, 1, Skv, Dk], index int64 (layout per cache_mode),
-    caches [d0, d1, 1, Dv] and [d0, d1, 1, Dk] (bf16/f16 like kv, or int8 /
-    float8_e4m3fn / float8_e5m2 with a float32 scale of length D* or 1).
-    `dev_status` (int32, 1 element) collects device-side error bits."""
+def _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ckv_scale, k_scale,
+             kc_scale, dev_status):
     _cuda(kv, "kv")
     Bkv, Skv, stride = _kv_rows(kv)
     if kv.dtype not in _IN_DTYPES:
@@ -117,7 +108,7 @@ def kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
             raise ValueError("%s must be float32" % name)
     if dev_status is not None and dev_status.dtype != torch.int32:
         raise ValueError("dev_status must be int32")
-    a = N.KvArgs(
+    return N.KvArgs(
         kv=kv.data_ptr(), in_dtype=_IN_DTYPES[kv.dtype], Bkv=Bkv, Skv=Skv, Dv=Dv, Dk=Dk,
         kv_row_stride=stride, gamma=_ptr(gamma, "gamma"), cos=_ptr(cos, "cos"),
         sin=_ptr(sin, "sin"), index=_ptr(index, "index"), mode=N.CACHE_MODES[cache_mode],
@@ -128,9 +119,54 @@ def kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
         k_cache=k_cache.data_ptr(), k_dtype=_CACHE_DTYPES[k_cache.dtype],
         k_scale=_ptr(k_scale, "k_scale"), k_scale_len=0 if k_scale is None else k_scale.numel(),
         eps=float(eps), kc_scale=float(kc_scale), dev_status=_ptr(dev_status, "dev_status"))
+
+
+def kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
+                          cache_mode="PA_BSND", eps=1e-6, ckv_scale=None, k_scale=None,
+                          kc_scale=1.0, dev_status=None, stream=None):
+    """Fused RMSNorm(kv[..., :Dv]) -> ckv_cache and interleaved RoPE(kv[..., Dv:]) ->
+    k_cache, scattered by `index` (-1 skips). Dv = gamma.numel().
+
+    kv [Bkv, 1, Skv, D] (bf16/f16; rows may be strided, e.g. a column slice),
+    cos/sin [Bkv, 1, Skv, Dk], index int64 (layout per cache_mode),
+    caches [d0, d1, 1, Dv] and [d0, d1, 1, Dk] (bf16/f16 like kv, or int8 /
+    float8_e4m3fn / float8_e5m2 with a float32 scale of length D* or 1).
+    `dev_status` (int32, 1 element) collects device-side error bits."""
+    a = _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ckv_scale,
+                 k_scale, kc_scale, dev_status)
     st = N.lib().kv_rmsnorm_rope_cache(ctypes.byref(a), _stream(stream))
     if st != N.KVR_OK:
         raise KvrError(st, "kv_rmsnorm_rope_cache")
+
+
+class PreparedCall:
+    """An entry point with its arguments marshalled once. Calling it launches
+    on `stream` (default: the current stream at call time) with the same
+    tensors, whose contents may change between calls; the caller keeps the
+    tensors alive and unmoved for the object's lifetime. For serving loops
+    that reuse fixed buffers every step: a call costs the C entry point only."""
+
+    def __init__(self, fn, args, name, keep):
+        self._fn = fn
+        self._args = args
+        self._ref = ctypes.byref(args)
+        self._name = name
+        self._keep = keep
+
+    def __call__(self, stream=None):
+        st = self._fn(self._ref, _stream(stream))
+        if st != N.KVR_OK:
+            raise KvrError(st, self._name)
+
+
+def prepare_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
+                                  cache_mode="PA_BSND", eps=1e-6, ckv_scale=None, k_scale=None,
+                                  kc_scale=1.0, dev_status=None):
+    """kv_rmsnorm_rope_cache with its arguments bound once (see PreparedCall)."""
+    a = _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ckv_scale,
+                 k_scale, kc_scale, dev_status)
+    keep = (kv, gamma, cos, sin, index, ckv_cache, k_cache, ckv_scale, k_scale, dev_status)
+    return PreparedCall(N.lib().kv_rmsnorm_rope_cache, a, "kv_rmsnorm_rope_cache", keep)
 
 
 def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,

@@ -7,7 +7,10 @@
 
 namespace kvr {
 
-constexpr int KV_THREADS = 128;
+#ifndef KVR_KV_THREADS
+#define KVR_KV_THREADS 128
+#endif
+constexpr int KV_THREADS = KVR_KV_THREADS;
 constexpr int KV_WARPS = KV_THREADS / 32;
 constexpr int64_t ROW_SKIP = -1;
 constexpr int64_t ROW_BAD = -2;

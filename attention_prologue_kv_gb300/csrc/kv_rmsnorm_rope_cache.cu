@@ -74,8 +74,19 @@ __device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane,
 #ifndef KVR_VEC_MIN_CTAS
 #define KVR_VEC_MIN_CTAS 8
 #endif
+// Small batches (the REG_GAMMA flavour) use 2-warp CTAs: the rows spread
+// over more SMs, which measured faster for a 256-row decode batch.
+template <bool REG_GAMMA>
+struct VecShape {
+    static constexpr int threads = REG_GAMMA ? 64 : KV_THREADS;
+    static constexpr int warps = threads / 32;
+};
+
 template <class IT, int CPL, int CK, bool REG_GAMMA>
-__global__ void __launch_bounds__(KV_THREADS, REG_GAMMA ? 6 : KVR_VEC_MIN_CTAS) kv_vec_kernel(const KvParams p) {
+__global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : KVR_VEC_MIN_CTAS)
+    kv_vec_kernel(const KvParams p) {
+    constexpr int WARPS = VecShape<REG_GAMMA>::warps;
+    constexpr int THREADS = VecShape<REG_GAMMA>::threads;
     extern __shared__ __align__(16) unsigned char smem[];
     const int nch = p.Dv >> 3;
     float4* g_lo = reinterpret_cast<float4*>(smem);
@@ -86,8 +97,8 @@ __global__ void __launch_bounds__(KV_THREADS, REG_GAMMA ? 6 : KVR_VEC_MIN_CTAS) 
 
     const int lane = threadIdx.x & 31;
     const int h = p.Dk >> 1;
-    const int64_t stride_rows = int64_t(gridDim.x) * KV_WARPS;
-    int64_t t = int64_t(blockIdx.x) * KV_WARPS + (threadIdx.x >> 5);
+    const int64_t stride_rows = int64_t(gridDim.x) * WARPS;
+    int64_t t = int64_t(blockIdx.x) * WARPS + (threadIdx.x >> 5);
 
     // While the preceding grid may still run, start this warp's first row on
     // its way from HBM into L2 (see prefetch_l2_bulk).
@@ -117,10 +128,10 @@ __global__ void __launch_bounds__(KV_THREADS, REG_GAMMA ? 6 : KVR_VEC_MIN_CTAS) 
         }
         kscale = (kq && p.k_scale_per_ch) ? p.k_scale : nullptr;
     } else {
-        stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, KV_THREADS);
-        if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, KV_THREADS);
+        stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, THREADS);
+        if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, THREADS);
         if (kq && p.k_scale_per_ch)
-            for (int i = threadIdx.x; i < p.Dk; i += KV_THREADS) s_kscale[i] = p.k_scale[i];
+            for (int i = threadIdx.x; i < p.Dk; i += THREADS) s_kscale[i] = p.k_scale[i];
         kscale = (kq && p.k_scale_per_ch) ? s_kscale : nullptr;
         __syncthreads();
     }
@@ -251,14 +262,14 @@ static VecKernel pick_cpl(int cpl, int ck, bool reg_gamma) {
 // Resident CTAs per SM for (kernel, dynamic shared memory), computed once and
 // cached: later calls (including calls under stream capture) make no query.
 // All devices this library runs on are the same architecture.
-static int ctas_per_sm(const void* fn, size_t smem) {
+static int ctas_per_sm(const void* fn, size_t smem, int threads = KV_THREADS) {
     static std::mutex mu;
     static std::map<std::pair<const void*, size_t>, int> cache;
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find({fn, smem});
     if (it != cache.end()) return it->second;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, KV_THREADS, smem) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         n = 1;
     }
@@ -279,9 +290,11 @@ cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, c
         VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind, reg_gamma)
                                             : pick_cpl<F16>(cpl, ckv_kind, reg_gamma);
         const size_t smem = reg_gamma ? 0 : size_t(p.Dv) * 8 + size_t(p.Dk) * 4;
-        const int64_t cap = int64_t(ctas_per_sm(reinterpret_cast<const void*>(fn), smem)) * sms;
-        const int grid = int(rows_ctas < cap ? rows_ctas : cap);
-        return launch_pdl(fn, dim3(grid), dim3(KV_THREADS), smem, s, p);
+        const int threads = reg_gamma ? VecShape<true>::threads : VecShape<false>::threads;
+        const int64_t ctas = (p.T + threads / 32 - 1) / (threads / 32);
+        const int64_t cap = int64_t(ctas_per_sm(reinterpret_cast<const void*>(fn), smem, threads)) * sms;
+        const int grid = int(ctas < cap ? ctas : cap);
+        return launch_pdl(fn, dim3(grid), dim3(threads), smem, s, p);
     }
     auto fn = in_dtype == KVR_BF16 ? kv_generic_kernel<BF16> : kv_generic_kernel<F16>;
     const int64_t cap = int64_t(ctas_per_sm(reinterpret_cast<const void*>(fn), 0)) * sms;

@@ -199,7 +199,10 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 // of shared memory.
 // ---------------------------------------------------------------------------
 
-constexpr int QSA_BULK_THREADS = 128;
+#ifndef KVR_QSA_BULK_THREADS
+#define KVR_QSA_BULK_THREADS 128
+#endif
+constexpr int QSA_BULK_THREADS = KVR_QSA_BULK_THREADS;
 
 template <class IT>
 __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaParams p) {
@@ -218,17 +221,18 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     const int tid = threadIdx.x;
 
     const int64_t per_seq = p.nbmax + 1;
+    const int64_t n = int64_t(blockIdx.x) / per_seq;
+    const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
+    __shared__ int64_t K_s;
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
-    __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
-
-    const int64_t n = int64_t(blockIdx.x) / per_seq;
-    const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
-    const int64_t K = p.key_length[p.key_length_per_seq ? n : 0];
+    if (tid == 0) K_s = p.key_length[p.key_length_per_seq ? n : 0];   // one load per CTA
+    __syncthreads();
+    const int64_t K = K_s;
     const int64_t P = K - p.L;
     if (P < 0) {
         if (jl == 0 && tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_KEY_LENGTH);

@@ -162,3 +162,28 @@ def test_rope_identity_on_gpu_is_exact_deinterleave():
     x = case.kv.reshape(-1, 576)[:, 512:].view(torch.int16).numpy().view(np.uint16)
     want = np.concatenate([x[:, 0::2], x[:, 1::2]], axis=1)
     assert np.array_equal(g_k.reshape(-1, 64)[case.index.numpy()], want)
+
+
+def test_prepared_call_matches_the_plain_call_and_sees_new_contents():
+    """A prepared call bound to fixed buffers: refilling the buffers between
+    calls gives each batch's own result."""
+    import attention_prologue_kv_gb300 as kvr
+    a = wl.make_kv_case("p", 4, 16, mode="PA_BSND", d0=16, d1=16, seed=60, skip=3)
+    b = wl.make_kv_case("p", 4, 16, mode="PA_BSND", d0=16, d1=16, seed=61, skip=2)
+    kv, cos, sin, idx = (a.kv.cuda(), a.cos.cuda(), a.sin.cuda(), a.index.cuda())
+    ckv = sentinel_cache((16, 16, 1, 512), "bf16")
+    k = sentinel_cache((16, 16, 1, 64), "bf16")
+    call = kvr.prepare_kv_rmsnorm_rope_cache(kv, a.gamma.cuda(), cos, sin, idx, ckv, k, cache_mode="PA_BSND")
+    call()
+    kv.copy_(b.kv)
+    cos.copy_(b.cos)
+    sin.copy_(b.sin)
+    idx.copy_(b.index)
+    b.gamma = a.gamma
+    call()
+    torch.cuda.synchronize()
+    r_ckv, r_k, _ = run_oracle_kv(a)
+    run_oracle_kv(b, r_ckv, r_k)
+    from helpers import codes_of
+    compare_cache(codes_of(ckv), r_ckv, "bf16", 512)
+    compare_cache(codes_of(k), r_k, "bf16", 64)
