@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(BULK_THREADS, 1) kv_bulk_kernel(const KvParams
 
     if (warp == 0) {
         // ---------------- producer ----------------
+        const uint64_t policy = l2_policy_evict_first();
         int64_t it = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
@@ -89,16 +90,16 @@ __global__ void __launch_bounds__(BULK_THREADS, 1) kv_bulk_kernel(const KvParams
             __syncwarp();
             const char* kvb = static_cast<const char*>(p.kv);
             if (p.kv_contig) {
-                if (lane == 0) bulk_g2s(st, kvb + r0 * kv_row, rows * kv_row, &full[s]);
+                if (lane == 0) bulk_g2s_hint(st, kvb + r0 * kv_row, rows * kv_row, &full[s], policy);
             } else {
                 for (int r = lane; r < rows; r += 32)
-                    bulk_g2s(st + r * kv_row, kvb + (r0 + r) * p.kv_stride * 2, kv_row, &full[s]);
+                    bulk_g2s_hint(st + r * kv_row, kvb + (r0 + r) * p.kv_stride * 2, kv_row, &full[s], policy);
             }
             if (lane == 1)
-                bulk_g2s(st + p.off_cos, static_cast<const char*>(p.cos) + r0 * cs_row, rows * cs_row, &full[s]);
+                bulk_g2s_hint(st + p.off_cos, static_cast<const char*>(p.cos) + r0 * cs_row, rows * cs_row, &full[s], policy);
             if (lane == 2)
-                bulk_g2s(st + p.off_sin, static_cast<const char*>(p.sin) + r0 * cs_row, rows * cs_row, &full[s]);
-            if (lane == 3 && idx_rows > 0) bulk_g2s(st + p.off_idx, p.index + r0, idx_rows * 8, &full[s]);
+                bulk_g2s_hint(st + p.off_sin, static_cast<const char*>(p.sin) + r0 * cs_row, rows * cs_row, &full[s], policy);
+            if (lane == 3 && idx_rows > 0) bulk_g2s_hint(st + p.off_idx, p.index + r0, idx_rows * 8, &full[s], policy);
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;
@@ -203,8 +204,15 @@ static BulkKernel pick_cpl(int cpl, int ck) {
 
 static uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Shared memory the ring may use per CTA (one CTA per SM).
-constexpr uint32_t BULK_RING_BYTES = 160 * 1024;
+// Shared memory the ring may use per CTA (one CTA per SM), and the largest
+// tile (rows per stage).
+#ifndef KVR_BULK_RING_KB
+#define KVR_BULK_RING_KB 160
+#endif
+#ifndef KVR_BULK_MAX_ROWS
+#define KVR_BULK_MAX_ROWS 32
+#endif
+constexpr uint32_t BULK_RING_BYTES = KVR_BULK_RING_KB * 1024;
 
 // Allow the kernel its dynamic shared memory once (not a stream operation,
 // so later calls under stream capture make no attribute call).
@@ -225,7 +233,7 @@ cudaError_t launch_kv_bulk(const KvParams& p0, int in_dtype, int ckv_kind, cudaS
     // batches so that the tiles still spread over the SMs.
     // Rows per tile: up to 16, fewer when that still leaves each CTA at least
     // four tiles (load balance across the SMs).
-    int R = 16;
+    int R = KVR_BULK_MAX_ROWS;
     while (R > 2 && (p.T + R - 1) / R < int64_t(4) * sms) R >>= 1;
     const uint32_t kv_row = uint32_t(p.Dv + p.Dk) * 2;
     const uint32_t cs_row = uint32_t(p.Dk) * 2;

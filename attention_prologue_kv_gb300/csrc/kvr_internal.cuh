@@ -160,6 +160,30 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// An L2 access policy that marks lines for early eviction (data read once),
+// and the bulk copy that carries it. KVR_BULK_EVICT_FIRST=0 uses the default
+// policy instead.
+#ifndef KVR_BULK_EVICT_FIRST
+#define KVR_BULK_EVICT_FIRST 1
+#endif
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+#if KVR_BULK_EVICT_FIRST
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+#else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+#endif
+    return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // L2 prefetch hints. They move nothing into registers or shared memory and
 // L2 is the point of coherence, so they may run before pdl_wait(): a write
 // by the preceding grid to a prefetched line still lands in L2 and is what

@@ -526,7 +526,7 @@ def run_extras(dev, kvr, wl, flush_buf):
         for f in calls:
             f()
         iso, _ = time_each(calls[0], 20, flush, stream)
-        steady = time_graph(calls, 8 * len(calls), stream)
+        steady = time_graph(calls, max(8 * len(calls), 48), stream)
         act = c0.active_tokens()
         nbytes = kv_algorithmic_bytes(act, c0.T - act, c0.Dv, c0.Dk,
                                       ckv_bytes=1 if c0.ckv_dtype != "bf16" else 2,
