@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(BULK_THREADS, 1) kv_bulk_kernel(const KvParams
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
             const int s = int(it % p.S);
-            if (it >= p.S && !mbar_wait(&empty[s], uint32_t(((it / p.S) - 1) & 1), abort_flag)) {
+            if (it >= p.S && !mbar_wait_warp(&empty[s], uint32_t(((it / p.S) - 1) & 1), abort_flag)) {
                 ok = false;
                 break;
             }
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(BULK_THREADS, 1) kv_bulk_kernel(const KvParams
         }
         // The CTA's shared memory must outlive every copy this warp issued.
         for (int64_t j = (it > p.S ? it - p.S : 0); j < it; ++j)
-            mbar_wait(&full[j % p.S], uint32_t((j / p.S) & 1), nullptr);
+            mbar_wait_warp(&full[j % p.S], uint32_t((j / p.S) & 1), nullptr);
         return;
     }
 
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(BULK_THREADS, 1) kv_bulk_kernel(const KvParams
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
         const int s = int(it % p.S);
-        if (!mbar_wait(&full[s], uint32_t((it / p.S) & 1), abort_flag)) {
+        if (!mbar_wait_warp(&full[s], uint32_t((it / p.S) & 1), abort_flag)) {
             if (lane == 0) {
                 *abort_flag = 1;
                 if (p.status != nullptr) atomicOr(p.status, KVR_DEVERR_TIMEOUT);

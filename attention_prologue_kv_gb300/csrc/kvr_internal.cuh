@@ -143,15 +143,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Wait until the phase with parity `parity` of `bar` has completed. Returns
 // false if *abort becomes non-zero (when abort is given) or WAIT_LIMIT_NS passes.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+// sleep_ns > 0 backs off between polls (for a lone waiter during a long copy,
+// so that it does not take issue slots from warps that are computing).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          unsigned sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
+        if (sleep_ns) __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
         if (abort != nullptr && *abort) return false;
         if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
     }
 }
+// mbar_wait for a whole warp: lane 0 waits, every lane gets its outcome, so
+// the warp never diverges on a wait that gives up.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                               unsigned sleep_ns = 0) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, sleep_ns) ? 1 : 0;
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
 // One bulk copy global -> shared, completion counted in bytes on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -220,40 +220,55 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     float* red = u + Di;                                                     // [QSA_BULK_THREADS/32 + 1]
     const int tid = threadIdx.x;
 
-    const int64_t per_seq = p.nbmax + 1;
-    const int64_t n = int64_t(blockIdx.x) / per_seq;
-    const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
-    __shared__ int64_t K_s;
+    // This CTA's candidate (sequence n, local block jl); 32-bit: the grid has
+    // fewer than 2^31 CTAs.
+    const uint32_t per_seq = uint32_t(p.nbmax + 1);
+    const uint32_t n32 = blockIdx.x / per_seq;
+    const int64_t n = n32;
+    const int64_t jl = int64_t(blockIdx.x - n32 * per_seq);
+    // The block's scalars, derived once by thread 0 (a 64-bit division is a
+    // long instruction sequence) and shared.
+    __shared__ int64_t sc[5];   // K, P, first block j0, completed blocks nb, status
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (tid == 0) K_s = p.key_length[p.key_length_per_seq ? n : 0];   // one load per CTA
+    if (tid == 0) {
+        const int64_t Kv = p.key_length[p.key_length_per_seq ? n : 0];
+        const int64_t Pv = Kv - p.L;
+        sc[0] = Kv;
+        sc[1] = Pv;
+        if (Pv >= 0) {
+            const int64_t j0v = Pv / kbs;
+            sc[2] = j0v;
+            sc[3] = Kv / kbs - j0v;
+        }
+    }
     __syncthreads();
-    const int64_t K = K_s;
-    const int64_t P = K - p.L;
+    const int64_t K = sc[0];
+    const int64_t P = sc[1];
     if (P < 0) {
         if (jl == 0 && tid == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_KEY_LENGTH);
         return;
     }
-    const int64_t F = P - P % kbs;
-    const int64_t j0 = P / kbs;
-    const int64_t nb = K / kbs - j0;
+    const int64_t j0 = sc[2];
+    const int64_t nb = sc[3];
+    const int64_t F = j0 * kbs;                  // first token of the incomplete block
     const uint16_t* raw = static_cast<const uint16_t*>(p.raw) + n * p.L * Di;
     const uint16_t* past = static_cast<const uint16_t*>(p.past_raw) + n * (kbs - 1) * Di;
 
     if (jl == p.nbmax) {
         // carry outputs (small; plain loads and stores)
-        const int64_t Fn = (K / kbs) * kbs;
-        const int64_t rem = K - Fn;
+        const int64_t Fn = (j0 + nb) * kbs;
+        const int rem = int(K - Fn);
         if (p.next_raw != nullptr) {
             uint16_t* dst = static_cast<uint16_t*>(p.next_raw) + n * (kbs - 1) * Di;
-            for (int64_t e = tid; e < rem * Di; e += QSA_BULK_THREADS) {
-                const int64_t r = e / Di, ch = e - r * Di;
+            for (int r = 0; r < rem; ++r) {
                 const int64_t tok = Fn + r;
-                dst[e] = tok < P ? past[(tok - F) * Di + ch] : raw[(tok - P) * Di + ch];
+                const uint16_t* src = tok < P ? past + (tok - F) * Di : raw + (tok - P) * Di;
+                for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) dst[int64_t(r) * Di + ch] = src[ch];
             }
         }
         if (p.next_rope != nullptr && p.Dr > 0 && rem > 0) {
@@ -303,9 +318,12 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     // Thread 0 waits for the copies; the rest of the CTA sleeps in the barrier
     // (which also orders thread 0's observation before every thread's reads).
     __shared__ int timed_out;
+#ifndef KVR_QSA_WAIT_SLEEP_NS
+#define KVR_QSA_WAIT_SLEEP_NS 128
+#endif
     if (tid == 0) {
         timed_out = 0;
-        if (!mbar_wait(bar, 0, nullptr)) {
+        if (!mbar_wait(bar, 0, nullptr, KVR_QSA_WAIT_SLEEP_NS)) {
             timed_out = 1;
             if (p.status != nullptr) atomicOr(p.status, KVR_DEVERR_TIMEOUT);
             mbar_wait(bar, 0, nullptr);   // the copies must land before the CTA exits
@@ -319,18 +337,21 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
         const int c = C >= QSA_BULK_THREADS ? cbase + tid : tid % C;
         const int g = C >= QSA_BULK_THREADS ? 0 : tid / C;
         if (c < C && g < G) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int64_t r = g; r < kbs; r += G) {
-                const uint4 v = *reinterpret_cast<const uint4*>(rows_s + r * row_b + c * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    acc[2 * k] += IT::lo(w[k]);
-                    acc[2 * k + 1] += IT::hi(w[k]);
-                }
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            const unsigned char* src = rows_s + c * 16;
+            const int nrow = int(kbs);
+#pragma unroll 4
+            for (int r = g; r < nrow; r += G) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + r * row_b);
+                acc[0] = __fadd2_rn(acc[0], make_float2(IT::lo(v.x), IT::hi(v.x)));
+                acc[1] = __fadd2_rn(acc[1], make_float2(IT::lo(v.y), IT::hi(v.y)));
+                acc[2] = __fadd2_rn(acc[2], make_float2(IT::lo(v.z), IT::hi(v.z)));
+                acc[3] = __fadd2_rn(acc[3], make_float2(IT::lo(v.w), IT::hi(v.w)));
             }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) part[g * Di + c * 8 + k] = acc[k];
+            float4* dst = reinterpret_cast<float4*>(part + g * Di + c * 8);
+            dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+            dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
         }
     }
     __syncthreads();
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) {
         float s = 0.f;
         for (int g = 0; g < G; ++g) s += part[g * Di + ch];
-        const float m = s / float(kbs);
+        const float m = s * p.inv_kbs;
         u[ch] = m;
         ss = fmaf(m, m, ss);
     }

@@ -90,3 +90,12 @@ def test_empty():
     case = wl.make_qsa_case("z", 3, 0, Di=32, Dr=8, kbs=4, seed=12)
     g_bk, _, _, st = run_gpu_qsa(case)
     assert st == 0 and np.all(g_bk == wl.SENTINEL16)
+
+
+@pytest.mark.parametrize("N,L,Di,Dr,kbs", [(3, 600, 128, 64, 128), (40, 300, 64, 16, 8)])
+def test_pipeline_ring_depths(N, L, Di, Dr, kbs):
+    """Shapes whose blocks go through a 4-stage ring (kbs = 128) and through an
+    8-stage ring with many blocks per CTA (the ring wraps many times)."""
+    case = wl.make_qsa_case("r", N, L, Di=Di, Dr=Dr, kbs=kbs, seed=N + L, past_max=500)
+    n, _ = check(case)
+    assert n == case.completed_blocks()
