@@ -56,7 +56,8 @@ def parse_args(argv=None):
                     help="CPU work budget of the oracle baseline leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--extras-only", action="store_true", help="time only the other workloads")
-    ap.add_argument("--only", choices=["prefill_paged", "quant_fp8", "tiny_norm", "qsa_prepare", "decode_paged"],
+    ap.add_argument("--only", choices=["prefill_paged", "quant_fp8", "tiny_norm", "qsa_prepare", "decode_paged",
+                                       "dynamic_quant_decode"],
                     help="run W + K launches of one workload and print their timing (for profilers)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
@@ -643,6 +644,11 @@ def run_only(args):
         a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
              d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
         fn = lambda: kvr.qsa_prepare(*a)
+    elif args.only == "dynamic_quant_decode":
+        q = wl.dynamic_quant_decode().to(dev)
+        o = torch.empty(q.shape, dtype=torch.int8, device=dev)
+        sc = torch.empty(q.shape[:-1] + (1,), dtype=torch.float32, device=dev)
+        fn = lambda: kvr.dynamic_quant(q, o, sc)
     else:
         case = getattr(wl, args.only)()
         ckv = torch.zeros(case.cache_shapes()[0], dtype=wl.code_torch_dtype(case.ckv_dtype), device=dev).view(

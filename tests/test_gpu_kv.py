@@ -187,3 +187,31 @@ def test_prepared_call_matches_the_plain_call_and_sees_new_contents():
     from helpers import codes_of
     compare_cache(codes_of(ckv), r_ckv, "bf16", 512)
     compare_cache(codes_of(k), r_k, "bf16", 64)
+
+
+def test_benchmark_decode_sets_match_the_oracle():
+    """The rotating decode batches the benchmark times, through the same
+    call and launch configuration, against the oracle (first four sets)."""
+    import attention_prologue_kv_gb300 as kvr
+    import oracle
+    from helpers import codes_of
+    sets = wl.decode_paged_sets(4)
+    d0, d1 = sets["d0"], sets["d1"]
+    ckv = sentinel_cache((d0, d1, 1, 512), "bf16")
+    k = sentinel_cache((d0, d1, 1, 64), "bf16")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r_ckv = np.full((d0, d1, 512), wl.SENTINEL16, dtype=np.uint16)
+    r_k = np.full((d0, d1, 64), wl.SENTINEL16, dtype=np.uint16)
+    g = sets["gamma"].cuda()
+    for i in range(4):
+        kvr.kv_rmsnorm_rope_cache(sets["kv"][i].cuda(), g, sets["cos"][i].cuda(), sets["sin"][i].cuda(),
+                                  sets["index"][i].cuda(), ckv, k, cache_mode="PA_BSND", dev_status=st)
+        oracle.ref_kv_rmsnorm_rope_cache(
+            sets["kv"][i].double().numpy().reshape(-1, 1, 576), sets["gamma"].double().numpy(),
+            sets["cos"][i].double().numpy().reshape(-1, 1, 64), sets["sin"][i].double().numpy().reshape(-1, 1, 64),
+            sets["index"][i].numpy(), r_ckv, r_k, Dv=512, mode="PA_BSND", eps=1e-6)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    n, _ = compare_cache(codes_of(ckv), r_ckv, "bf16", 512)
+    assert n == 4 * 251
+    compare_cache(codes_of(k), r_k, "bf16", 64)
