@@ -33,19 +33,48 @@ __device__ __forceinline__ int dq_code(float x, float s) {
     return min(max(c, -127), 127);
 }
 
-// The same code without a division per element. With y = RN(1/s), the
-// product q0 = RN(x*y) differs from x/s by at most (2^-24 + 2^-24 + 2^-48)|x/s|
-// and from fl32(x/s) by less than 3 ulps of q0, i.e. by less than 2^-16 for
-// |q0| < 128 (codes are at most 127 in magnitude, ulp(q0) <= 2^-17 there).
-// Rounding q0 or fl32(x/s) to an integer can therefore differ only when q0
-// lies within that distance of a half-integer; those elements (rare) take the
-// IEEE division. Valid while 1/s is a normal float: the caller checks
-// s >= 2^-100 for the row.
-__device__ __forceinline__ int dq_code_fast(float x, float s, float y) {
-    const float q0 = x * y;
-    const float r0 = rintf(q0);
-    if (fabsf(fabsf(q0 - r0) - 0.5f) > 0x1p-15f) return min(max(int(r0), -127), 127);
-    return dq_code(x, s);
+// Eight codes of one 16-byte chunk at once, packed into 8 bytes, without a
+// division per element. With y = RN(1/s), the product q0 = RN(x*y) differs
+// from x/s by at most (2^-24 + 2^-24 + 2^-48)|x/s| and from fl32(x/s) by less
+// than 3 ulps of q0, i.e. by less than 2^-16 for |q0| < 128 (codes are at
+// most 127 in magnitude, ulp(q0) <= 2^-17 there). Rounding q0 or fl32(x/s)
+// to an integer can therefore differ only when q0 lies within that distance
+// of a half-integer: `mind` tracks the smallest such distance, and the caller
+// recomputes the lane's codes by IEEE division when it is 2^-15 or less.
+// Valid while 1/s is a normal float (the caller checks s >= 2^-100).
+// Rounding: with M = 1.5 * 2^23, t = fl(q0 + M) rounds q0 (|q0| < 2^22) to an
+// integer with ties to even inside the addition, and the low byte of t's bits
+// is that integer's two's-complement byte.
+template <class IT>
+__device__ __forceinline__ uint2 dq_chunk_fast(const uint4& x, float y, float& mind) {
+    const float M = 12582912.0f;
+    const float2 y2 = make_float2(y, y), M2 = make_float2(M, M), nM2 = make_float2(-M, -M),
+                 m1 = make_float2(-1.f, -1.f);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 q0 = __fmul2_rn(make_float2(IT::lo(w[k]), IT::hi(w[k])), y2);
+        const float2 t = __fadd2_rn(q0, M2);
+        const float2 r = __fadd2_rn(t, nM2);          // rint(q0), exact
+        const float2 d = __ffma2_rn(r, m1, q0);       // q0 - r, exact
+        mind = fminf(mind, fminf(fabsf(fabsf(d.x) - 0.5f), fabsf(fabsf(d.y) - 0.5f)));
+        b[k] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);   // two code bytes
+    }
+    return make_uint2(__byte_perm(b[0], b[1], 0x5410), __byte_perm(b[2], b[3], 0x5410));
+}
+
+// The same eight codes with one IEEE division each (exact reference path).
+template <class IT>
+__device__ __forceinline__ uint2 dq_chunk_exact(const uint4& x, float s) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t b[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        b[2 * k] = uint32_t(dq_code(IT::lo(w[k]), s)) & 0xFFu;
+        b[2 * k + 1] = uint32_t(dq_code(IT::hi(w[k]), s)) & 0xFFu;
+    }
+    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
 // max(|a|, |b|) over the two 16-bit lanes of w, exact: clear the sign bits and
@@ -108,23 +137,22 @@ __global__ void __launch_bounds__(DQ_THREADS) dq_vec_kernel(const DqParams p) {
         const bool fast = s >= 0x1p-100f;
         const float y = fast ? __frcp_rn(s) : 0.f;
         char* dst = reinterpret_cast<char*>(p.out) + t * p.H;
+        uint2 o[CPL];
+        float mind = 1.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            if (c * 32 + lane < nch) o[c] = fast ? dq_chunk_fast<IT>(x[c], y, mind) : dq_chunk_exact<IT>(x[c], s);
+        // Any product within 2^-15 of a half-integer: this lane's codes again,
+        // by IEEE division (rare).
+        if (fast && !(mind > 0x1p-15f)) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+                if (c * 32 + lane < nch) o[c] = dq_chunk_exact<IT>(x[c], s);
+        }
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
             const int ch = c * 32 + lane;
-            if (ch < nch) {
-                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
-                uint32_t b[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float lo = IT::lo(w[k]), hi = IT::hi(w[k]);
-                    b[2 * k] = uint32_t(fast ? dq_code_fast(lo, s, y) : dq_code(lo, s)) & 0xFFu;
-                    b[2 * k + 1] = uint32_t(fast ? dq_code_fast(hi, s, y) : dq_code(hi, s)) & 0xFFu;
-                }
-                uint2 o;
-                o.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                o.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-                *reinterpret_cast<uint2*>(dst + ch * 8) = o;
-            }
+            if (ch < nch) *reinterpret_cast<uint2*>(dst + ch * 8) = o[c];
         }
         if (lane == 0) p.scale[t] = s;
 #pragma unroll
@@ -170,10 +198,10 @@ static int dq_ctas_per_sm(const void* fn) {
 cudaError_t launch_dq(const DqParams& p, int in_dtype, bool vec, cudaStream_t s) {
     const int64_t ctas = (p.rows + DQ_WARPS - 1) / DQ_WARPS;
     const int sms = sm_count_current_device();
+    typedef void (*K)(const DqParams);
     if (vec) {
         const int nch = int(p.H / 8);
         const int cpl = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
-        typedef void (*K)(const DqParams);
         K fn;
         if (in_dtype == KVR_BF16)
             fn = cpl == 1 ? dq_vec_kernel<BF16, 1> : (cpl == 2 ? dq_vec_kernel<BF16, 2> : dq_vec_kernel<BF16, 4>);
