@@ -29,6 +29,20 @@ Readings where the page is silent (each also listed with the design notes):
   bfloat16 at the end.
 * Carry-out (for chaining calls): the raw keys of the tokens after the last
   completed block, and the cos/sin of the first of them.
+
+Variants the page leaves open, each selectable (the defaults are the readings
+above):
+* rope_layout: which Dr channels rotate (the last or the first) and how the
+  pairs are formed: "interleave" takes (x[2i], x[2i+1]) as in the
+  aclnnKvRmsNormRopeCache formula; "half" takes (x[i], x[i + Dr/2]), the
+  rotate-half form. Both write the pair's results to lanes i and i + Dr/2
+  with the same cos/sin lanes.
+* past_block_keys (concat-output form): the output is a fresh buffer; the
+  rows j < floor(P/kbs) come from past_block_index_keys [N, Bp, Di], so the
+  result is the past block keys followed by the new ones. Rows the past
+  buffer does not hold (Bp < floor(P/kbs)) are left untouched and raise
+  STATUS_PAST_BLOCKS; past rows that fall at or beyond Bcap raise
+  STATUS_BLOCK_CAP.
 """
 import numpy as np
 
@@ -37,17 +51,45 @@ from .kv_rmsnorm_rope_cache import interleave_rope, rms_norm
 
 STATUS_KEY_LENGTH = 0x2   # key_length[n] < L
 STATUS_BLOCK_CAP = 0x4    # a completed block's index is beyond the block-key buffer
+STATUS_PAST_BLOCKS = 0x10  # past_block_index_keys holds fewer rows than floor(P/kbs)
+
+ROPE_LAYOUTS = ("interleave_last", "interleave_first", "half_last", "half_first")
+
+
+def rotate_half_rope(x, cos, sin):
+    """RoPE in the rotate-half form over the last axis: x1 = first half,
+    x2 = second half, y = cat(x1,x2)*cos + cat(-x2,x1)*sin."""
+    h = x.shape[-1] // 2
+    x1 = x[..., :h]
+    x2 = x[..., h:]
+    return np.concatenate((x1, x2), axis=-1) * cos + np.concatenate((-x2, x1), axis=-1) * sin
+
+
+def rotate_channels(u, c, s, layout):
+    """Apply the RoPE of `layout` (one of ROPE_LAYOUTS) to the Dr channels it
+    names (Dr = len(c)); the other channels pass through."""
+    Dr = len(c)
+    style, where = layout.split("_")
+    rope = interleave_rope if style == "interleave" else rotate_half_rope
+    if where == "last":
+        return np.concatenate((u[:len(u) - Dr], rope(u[len(u) - Dr:], c, s)))
+    return np.concatenate((rope(u[:Dr], c, s), u[Dr:]))
 
 
 def ref_qsa_prepare(raw, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,
                     past_raw, past_rope, key_block_size, eps=1e-6,
-                    next_raw=None, next_rope=None, out_dtype="bf16"):
+                    next_raw=None, next_rope=None, out_dtype="bf16",
+                    rope_layout="interleave_last", past_block_keys=None):
     """raw [N, L, Di] f64; block_keys codes [N, Bcap, Di] (written in place);
     key_length int [N] or [1]; rope_cos/rope_sin [N, L, Dr] f64 or None;
     k_norm_weight [Di] f64 or None; past_raw [N, kbs-1, Di] f64;
     past_rope [N, 2*Dr] f64 or None; next_raw [N, kbs-1, Di] f64 / next_rope
-    [N, 2*Dr] f64 optional carry outputs (written in place).
+    [N, 2*Dr] f64 optional carry outputs (written in place); rope_layout
+    one of ROPE_LAYOUTS; past_block_keys codes [N, Bp, Di] or None (None:
+    block_keys already holds the past keys).
     Returns the device-status bits the call would raise."""
+    if rope_layout not in ROPE_LAYOUTS:
+        raise ValueError(rope_layout)
     N, L, Di = raw.shape
     kbs = int(key_block_size)
     Bcap = block_keys.shape[1]
@@ -62,6 +104,15 @@ def ref_qsa_prepare(raw, block_keys, key_length, rope_cos, rope_sin, k_norm_weig
             continue
         f = P % kbs
         F = P - f
+        if past_block_keys is not None:
+            Bp = past_block_keys.shape[1]
+            if Bp < P // kbs:
+                status |= STATUS_PAST_BLOCKS
+            for j in range(min(Bp, P // kbs)):
+                if j >= Bcap:
+                    status |= STATUS_BLOCK_CAP
+                    break
+                block_keys[n, j] = past_block_keys[n, j]
 
         def key(p):
             return past_raw[n, p - F] if p < P else raw[n, p - P]
@@ -76,7 +127,7 @@ def ref_qsa_prepare(raw, block_keys, key_length, rope_cos, rope_sin, k_norm_weig
             u = m if k_norm_weight is None else rms_norm(m, k_norm_weight, eps)
             if rope_cos is not None:
                 c, s = rope_at(j * kbs)
-                u = np.concatenate((u[:Di - Dr], interleave_rope(u[Di - Dr:], c, s)))
+                u = rotate_channels(u, c, s, rope_layout)
             if j >= Bcap:
                 status |= STATUS_BLOCK_CAP
                 continue

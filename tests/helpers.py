@@ -77,7 +77,9 @@ def oracle_qsa_inputs(case):
                 past_rope=f64(case.past_rope), key_block_size=case.kbs, eps=case.eps)
 
 
-def run_oracle_qsa(case, block_keys=None, carry=False):
+def run_oracle_qsa(case, block_keys=None, carry=False, rope_layout="interleave_last",
+                   past_block_keys=None):
+    """past_block_keys: codes [N, Bp, Di] (numpy) for the concat-output form."""
     import oracle
     from attention_prologue_kv_gb300.workloads import SENTINEL16
     if block_keys is None:
@@ -87,6 +89,7 @@ def run_oracle_qsa(case, block_keys=None, carry=False):
         nr = np.full((case.N, case.kbs - 1, case.Di), np.nan)
         npr = np.full((case.N, 2 * case.Dr), np.nan) if case.Dr else None
     st = oracle.ref_qsa_prepare(block_keys=block_keys, next_raw=nr, next_rope=npr,
+                                rope_layout=rope_layout, past_block_keys=past_block_keys,
                                 **oracle_qsa_inputs(case))
     return block_keys, nr, npr, st
 
@@ -152,7 +155,9 @@ def compare_cache(gpu, ref, dtype, D):
     return int(written.sum()), float(np.mean(gw == rw)) if gw.size else 1.0
 
 
-def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda"):
+def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="interleave_last",
+                past_block_keys=None):
+    """past_block_keys: codes [N, Bp, Di] (numpy) for the concat-output form."""
     import attention_prologue_kv_gb300 as kvr
     from attention_prologue_kv_gb300.workloads import SENTINEL16
     bk = block_keys
@@ -168,6 +173,9 @@ def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda"):
     d = lambda t: None if t is None else t.to(dev)
     kvr.qsa_prepare(d(case.raw), bk, d(case.key_length), d(case.rope_cos), d(case.rope_sin),
                     d(case.k_norm_weight), d(case.past_raw), d(case.past_rope), case.kbs, case.eps,
-                    next_incomplete_raw_keys=nr, next_incomplete_rope=npr, dev_status=status)
+                    next_incomplete_raw_keys=nr, next_incomplete_rope=npr, dev_status=status,
+                    rope_layout=rope_layout,
+                    past_block_index_keys=None if past_block_keys is None else
+                    torch.from_numpy(past_block_keys.view(np.int16)).to(dev).view(case.raw.dtype))
     torch.cuda.synchronize()
     return codes_of(bk), f64(nr), f64(npr), int(status.item())

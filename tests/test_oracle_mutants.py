@@ -53,9 +53,38 @@ NORM_MUTANTS = {
 }
 
 
+def _half_rope_pins(rope):
+    """True if `rope` (rotate-half form) passes the complex-rotation closed form
+    with a distinct angle per pair, and the identity and quarter-turn cases."""
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((3, 16))
+    th = rng.uniform(-np.pi, np.pi, (3, 8))
+    c = np.concatenate((np.cos(th), np.cos(th)), -1)
+    s = np.concatenate((np.sin(th), np.sin(th)), -1)
+    y = rope(x, c, s)
+    ok = np.allclose(y[:, :8] + 1j * y[:, 8:], (x[:, :8] + 1j * x[:, 8:]) * np.exp(1j * th), rtol=1e-13, atol=1e-14)
+    ok &= np.array_equal(rope(x, np.ones(16), np.zeros(16)), x)
+    ok &= np.array_equal(rope(x, np.zeros(16), np.ones(16)), np.concatenate([-x[:, 8:], x[:, :8]], -1))
+    return bool(ok)
+
+
+HALF_ROPE_MUTANTS = {
+    "interleave instead of rotate-half": oracle.interleave_rope,
+    "sign on the wrong half": lambda x, c, s: x * c + _cat(x[..., x.shape[-1] // 2:], -x[..., :x.shape[-1] // 2]) * s,
+    "cos of the neighbouring lane": lambda x, c, s: oracle.rotate_half_rope(x, np.roll(c, 1, -1), s),
+    "halves not swapped in the sin term": lambda x, c, s: x * c + x * s,
+}
+
+
 def test_true_oracle_passes_the_pins():
     assert _rope_pins(oracle.interleave_rope)
+    assert _half_rope_pins(oracle.rotate_half_rope)
     assert _norm_pins(oracle.rms_norm)
+
+
+@pytest.mark.parametrize("name", sorted(HALF_ROPE_MUTANTS))
+def test_half_rope_mutant_is_caught(name):
+    assert not _half_rope_pins(HALF_ROPE_MUTANTS[name])
 
 
 @pytest.mark.parametrize("name", sorted(ROPE_MUTANTS))

@@ -153,3 +153,106 @@ def test_rope_uses_first_token_of_block_on_last_dr_channels():
     bk3, _, _, _ = run_oracle_qsa(c3)
     assert np.array_equal(bk3[0, 1, :8], bk[0, 1, :8])
     assert not np.array_equal(bk3[0, 1, 8:], bk[0, 1, 8:])
+
+
+# ---- RoPE layouts (which Dr channels rotate, and how pairs are formed) ----
+
+def _no_rope(case):
+    import dataclasses
+    return dataclasses.replace(case, rope_cos=None, rope_sin=None, past_rope=None, Dr=0)
+
+
+@pytest.mark.parametrize("layout", oracle.ROPE_LAYOUTS)
+def test_rope_layout_rotates_only_its_channels(layout):
+    """Against the same call with the rotation disabled: the Dr channels the
+    layout names change, the others are bit-identical."""
+    case = wl.make_qsa_case("t", 3, 40, Di=24, Dr=8, kbs=4, seed=21, past=[0, 3, 9])
+    bk, _, _, st = run_oracle_qsa(case, rope_layout=layout)
+    plain, _, _, _ = run_oracle_qsa(_no_rope(case))
+    assert st == 0
+    rot = slice(0, 8) if layout.endswith("first") else slice(16, 24)
+    keep = slice(8, 24) if layout.endswith("first") else slice(0, 16)
+    written = ~np.all(plain == wl.SENTINEL16, axis=-1)
+    assert written.sum() == case.completed_blocks()
+    assert np.array_equal(bk[..., keep], plain[..., keep])
+    assert not np.array_equal(bk[written][:, rot], plain[written][:, rot])
+
+
+@pytest.mark.parametrize("layout", oracle.ROPE_LAYOUTS)
+def test_rope_layout_identity_and_quarter_turn(layout):
+    """cos = 1, sin = 0 on every table: the rotate-half layouts leave the key
+    unchanged, the interleaved ones de-interleave the rotated channels.
+    cos = 0, sin = 1: pair (a, b) becomes (-b, a) in both, pairs taken by
+    each layout's own rule."""
+    case = wl.make_qsa_case("t", 2, 24, Di=16, Dr=8, kbs=4, seed=22, past=[0, 2], norm=False)
+    plain, _, _, _ = run_oracle_qsa(_no_rope(case))
+    v = enc.bf16_decode(plain)
+    rot = slice(0, 8) if layout.endswith("first") else slice(8, 16)
+    x = v[..., rot]
+    if layout.startswith("half"):
+        x1, x2 = x[..., :4], x[..., 4:]
+    else:
+        x1, x2 = x[..., 0::2], x[..., 1::2]
+    for cv, sv, want in ((1.0, 0.0, np.concatenate((x1, x2), -1)), (0.0, 1.0, np.concatenate((-x2, x1), -1))):
+        for t in (case.rope_cos, case.rope_sin, case.past_rope):
+            t.fill_(0)
+        case.rope_cos.fill_(cv)
+        case.rope_sin.fill_(sv)
+        case.past_rope[:, :8] = cv
+        case.past_rope[:, 8:] = sv
+        bk, _, _, _ = run_oracle_qsa(case, rope_layout=layout)
+        got = enc.bf16_decode(bk)
+        written = ~np.all(plain == wl.SENTINEL16, axis=-1)
+        np.testing.assert_array_equal(got[written][:, rot], want[written])
+
+
+def test_rotate_half_is_interleave_of_the_paired_lanes():
+    """The two pairings differ only by which lanes form a pair: rotate-half on
+    x equals the interleaved RoPE on x with its halves interleaved."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((5, 12))
+    c, s = rng.standard_normal((2, 5, 12))
+    xi = np.empty_like(x)
+    xi[:, 0::2], xi[:, 1::2] = x[:, :6], x[:, 6:]
+    np.testing.assert_allclose(oracle.rotate_half_rope(x, c, s), oracle.interleave_rope(xi, c, s),
+                               rtol=0, atol=0)
+
+
+# ---- concat-output form (past_block_index_keys as a separate input) ----
+
+def _past_codes(case, Bp, seed):
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, 0x7F00, (case.N, Bp, case.Di), dtype=np.uint16)
+
+
+def test_concat_form_is_past_prefix_then_new_blocks():
+    """Fresh output: rows j < floor(P/kbs) are the past keys bit for bit, the
+    new blocks equal the in-place call's, rows of the past buffer at or
+    beyond floor(P/kbs) are not copied, and everything else stays untouched."""
+    case = wl.make_qsa_case("t", 3, 30, Di=16, Dr=8, kbs=4, seed=24, past=[0, 9, 17], Bcap=14)
+    past = _past_codes(case, 6, 1)
+    bk, _, _, st = run_oracle_qsa(case, past_block_keys=past)
+    inplace, _, _, _ = run_oracle_qsa(case)
+    assert st == 0
+    for n, P in enumerate(case.meta["past"]):
+        j0 = P // case.kbs
+        assert np.array_equal(bk[n, :j0], past[n, :j0])
+        assert np.array_equal(bk[n, j0:], inplace[n, j0:])
+
+
+def test_concat_form_short_past_buffer_raises_status():
+    case = wl.make_qsa_case("t", 2, 12, Di=16, Dr=8, kbs=4, seed=25, past=[4, 20], Bcap=10)
+    past = _past_codes(case, 3, 2)       # sequence 1 has floor(20/4) = 5 past blocks
+    bk, _, _, st = run_oracle_qsa(case, past_block_keys=past)
+    assert st == oracle.STATUS_PAST_BLOCKS
+    assert np.array_equal(bk[1, :3], past[1])
+    assert np.all(bk[1, 3:5] == wl.SENTINEL16)
+    assert np.array_equal(bk[0, :1], past[0, :1]) and np.all(bk[0, 1] != wl.SENTINEL16)
+
+
+def test_concat_form_past_beyond_capacity_raises_block_cap():
+    case = wl.make_qsa_case("t", 1, 4, Di=16, Dr=8, kbs=4, seed=26, past=[16], Bcap=3)
+    past = _past_codes(case, 4, 3)
+    bk, _, _, st = run_oracle_qsa(case, past_block_keys=past)
+    assert st == oracle.STATUS_BLOCK_CAP
+    assert np.array_equal(bk[0], past[0, :3])
