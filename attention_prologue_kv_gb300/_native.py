@@ -5,6 +5,7 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvr.so")
+ABI_VERSION = 2   # KVR_ABI_VERSION of include/kvr.h these structures mirror
 
 # kvr_status
 KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS, KVR_ERR_CUDA = range(7)
@@ -12,6 +13,10 @@ KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS,
 KVR_DEVERR_INDEX = 0x1
 KVR_DEVERR_KEY_LENGTH = 0x2
 KVR_DEVERR_BLOCK_CAP = 0x4
+KVR_DEVERR_TIMEOUT = 0x8
+KVR_DEVERR_PAST_BLOCKS = 0x10
+# kvr_qsa_rope
+QSA_ROPE_LAYOUTS = {"interleave_last": 0, "interleave_first": 1, "half_last": 2, "half_first": 3}
 # kvr_dtype
 KVR_BF16, KVR_F16, KVR_INT8, KVR_FP8_E4M3FN, KVR_FP8_E5M2 = range(5)
 # kvr_cache_mode
@@ -49,6 +54,7 @@ class QsaArgs(ctypes.Structure):
         ("key_block_size", _i64), ("eps", _f32),
         ("next_incomplete_raw_keys", _vp), ("next_incomplete_rope", _vp),
         ("dev_status", _vp),
+        ("rope_layout", _int), ("past_block_index_keys", _vp), ("Bp", _i64),
     ]
 
 
@@ -90,6 +96,9 @@ def lib():
     L.kvr_status_string.restype = ctypes.c_char_p
     L.kvr_abi_version.argtypes = []
     L.kvr_abi_version.restype = _int
+    if L.kvr_abi_version() != ABI_VERSION:
+        raise RuntimeError("libkvr.so has ABI version %d, the binding expects %d: rebuild it with "
+                           "`python -m attention_prologue_kv_gb300.build`" % (L.kvr_abi_version(), ABI_VERSION))
     _lib = L
     return L
 

@@ -172,14 +172,18 @@ def prepare_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache
 def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,
                 past_incomplete_raw_keys, past_incomplete_rope, key_block_size, epsilon=1e-6, *,
                 next_incomplete_raw_keys=None, next_incomplete_rope=None, dev_status=None,
-                stream=None):
+                rope_layout="interleave_last", past_block_index_keys=None, stream=None):
     """QSA block-key prepare. Positional arguments follow the qsa_prepare
     parameter list; `block_keys` [N, Bcap, Di] holds the past block keys and
     receives the new ones in place (block j at row j). rope_cos/rope_sin
     [N, L, Dr] (or both None), k_norm_weight [Di] or None,
     past_incomplete_raw_keys [N, kbs-1, Di], past_incomplete_rope [N, 2*Dr] or
     None, key_length int64 [N] or [1] = valid tokens after this call.
-    Optional carry outputs next_incomplete_raw_keys / next_incomplete_rope."""
+    Optional carry outputs next_incomplete_raw_keys / next_incomplete_rope.
+    rope_layout: "interleave_last" (default), "interleave_first", "half_last"
+    or "half_first" (which Dr channels rotate; interleaved or rotate-half
+    pairs). past_block_index_keys [N, Bp, Di]: concat-output form, its rows
+    j < floor(P/kbs) are copied into block_keys first."""
     raw = _cuda(raw_index_keys, "raw_index_keys")
     if raw.dim() != 3:
         raise ValueError("raw_index_keys must be [N, L, Di]")
@@ -194,9 +198,18 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
                     (past_incomplete_raw_keys, "past_incomplete_raw_keys"),
                     (past_incomplete_rope, "past_incomplete_rope"),
                     (next_incomplete_raw_keys, "next_incomplete_raw_keys"),
-                    (next_incomplete_rope, "next_incomplete_rope")):
+                    (next_incomplete_rope, "next_incomplete_rope"),
+                    (past_block_index_keys, "past_block_index_keys")):
         if t is not None and t.dtype != raw.dtype:
             raise ValueError("%s must have raw_index_keys' dtype" % name)
+    if rope_layout not in N.QSA_ROPE_LAYOUTS:
+        raise ValueError("rope_layout must be one of %s" % sorted(N.QSA_ROPE_LAYOUTS))
+    Bp = 0
+    if past_block_index_keys is not None:
+        if past_block_index_keys.dim() != 3 or past_block_index_keys.shape[0] != Nn or \
+                past_block_index_keys.shape[2] != Di:
+            raise ValueError("past_block_index_keys must be [N, Bp, Di]")
+        Bp = past_block_index_keys.shape[1]
     if dev_status is not None and dev_status.dtype != torch.int32:
         raise ValueError("dev_status must be int32")
     Dr = rope_cos.shape[-1] if rope_cos is not None else 0
@@ -211,7 +224,8 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
         key_block_size=int(key_block_size), eps=float(epsilon),
         next_incomplete_raw_keys=_ptr(next_incomplete_raw_keys, "next_incomplete_raw_keys"),
         next_incomplete_rope=_ptr(next_incomplete_rope, "next_incomplete_rope"),
-        dev_status=_ptr(dev_status, "dev_status"))
+        dev_status=_ptr(dev_status, "dev_status"), rope_layout=N.QSA_ROPE_LAYOUTS[rope_layout],
+        past_block_index_keys=_ptr(past_block_index_keys, "past_block_index_keys"), Bp=Bp)
     if block_keys.shape[0] != Nn or block_keys.shape[2] != Di:
         raise ValueError("block_keys must be [N, Bcap, Di]")
     st = N.lib().qsa_prepare(ctypes.byref(a), _stream(stream))

@@ -9,8 +9,9 @@
 // and a warp butterfly (exact); the scale is one IEEE division; each code is
 // the IEEE quotient rounded to nearest even (the float32 operations the
 // formula names), obtained from a reciprocal product except near rounding
-// boundaries (dq_code_fast); each lane stores 8 codes with one 8-byte store. The first row of each warp is
-// prefetched into L2 before the programmatic-dependent-launch wait.
+// boundaries (dq_chunk_fast); each lane stores 8 codes with one 8-byte store.
+// The first row of each warp is prefetched into L2 before the
+// programmatic-dependent-launch wait.
 #include <map>
 #include <mutex>
 
@@ -39,14 +40,16 @@ __device__ __forceinline__ int dq_code(float x, float s) {
 // than 3 ulps of q0, i.e. by less than 2^-16 for |q0| < 128 (codes are at
 // most 127 in magnitude, ulp(q0) <= 2^-17 there). Rounding q0 or fl32(x/s)
 // to an integer can therefore differ only when q0 lies within that distance
-// of a half-integer: `mind` tracks the smallest such distance, and the caller
-// recomputes the lane's codes by IEEE division when it is 2^-15 or less.
+// of a half-integer. With d = q0 - rint(q0) (|d| <= 1/2), the distance to the
+// nearest half-integer is 1/2 - |d|: `maxd` tracks the largest |d|, and the
+// caller recomputes the lane's codes by IEEE division when it reaches
+// 1/2 - 2^-15.
 // Valid while 1/s is a normal float (the caller checks s >= 2^-100).
 // Rounding: with M = 1.5 * 2^23, t = fl(q0 + M) rounds q0 (|q0| < 2^22) to an
 // integer with ties to even inside the addition, and the low byte of t's bits
 // is that integer's two's-complement byte.
 template <class IT>
-__device__ __forceinline__ uint2 dq_chunk_fast(const uint4& x, float y, float& mind) {
+__device__ __forceinline__ uint2 dq_chunk_fast(const uint4& x, float y, float& maxd) {
     const float M = 12582912.0f;
     const float2 y2 = make_float2(y, y), M2 = make_float2(M, M), nM2 = make_float2(-M, -M),
                  m1 = make_float2(-1.f, -1.f);
@@ -58,7 +61,7 @@ __device__ __forceinline__ uint2 dq_chunk_fast(const uint4& x, float y, float& m
         const float2 t = __fadd2_rn(q0, M2);
         const float2 r = __fadd2_rn(t, nM2);          // rint(q0), exact
         const float2 d = __ffma2_rn(r, m1, q0);       // q0 - r, exact
-        mind = fminf(mind, fminf(fabsf(fabsf(d.x) - 0.5f), fabsf(fabsf(d.y) - 0.5f)));
+        maxd = fmaxf(maxd, fmaxf(fabsf(d.x), fabsf(d.y)));
         b[k] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);   // two code bytes
     }
     return make_uint2(__byte_perm(b[0], b[1], 0x5410), __byte_perm(b[2], b[3], 0x5410));
@@ -138,13 +141,13 @@ __global__ void __launch_bounds__(DQ_THREADS) dq_vec_kernel(const DqParams p) {
         const float y = fast ? __frcp_rn(s) : 0.f;
         char* dst = reinterpret_cast<char*>(p.out) + t * p.H;
         uint2 o[CPL];
-        float mind = 1.f;
+        float maxd = 0.f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
-            if (c * 32 + lane < nch) o[c] = fast ? dq_chunk_fast<IT>(x[c], y, mind) : dq_chunk_exact<IT>(x[c], s);
+            if (c * 32 + lane < nch) o[c] = fast ? dq_chunk_fast<IT>(x[c], y, maxd) : dq_chunk_exact<IT>(x[c], s);
         // Any product within 2^-15 of a half-integer: this lane's codes again,
         // by IEEE division (rare).
-        if (fast && !(mind > 0x1p-15f)) {
+        if (fast && !(maxd < 0.5f - 0x1p-15f)) {
 #pragma unroll
             for (int c = 0; c < CPL; ++c)
                 if (c * 32 + lane < nch) o[c] = dq_chunk_exact<IT>(x[c], s);

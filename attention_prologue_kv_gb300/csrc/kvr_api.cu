@@ -3,6 +3,8 @@
 // are invalid; see include/kvr.h for the contract.
 #include <mutex>
 
+#include <algorithm>
+
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -190,43 +192,59 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
 kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
     if (a == nullptr) return KVR_ERR_NULL;
     if (!is16(a->in_dtype)) return KVR_ERR_DTYPE;
-    const bool rope = a->rope_cos != nullptr || a->rope_sin != nullptr;
+    if (a->rope_layout < KVR_QSA_ROPE_INTERLEAVE_LAST || a->rope_layout > KVR_QSA_ROPE_HALF_FIRST)
+        return KVR_ERR_MODE;
+    // With no new tokens (L = 0) the tables are never read and may be NULL:
+    // the rotation is then on iff the carried cos/sin is given.
+    const bool rope = a->rope_cos != nullptr || a->rope_sin != nullptr ||
+                      (a->L == 0 && a->past_incomplete_rope != nullptr);
     if (a->N < 0 || a->L < 0 || a->Di < 1 || a->Di > 4096 || a->Bcap < 1 || a->key_block_size < 2 ||
-        (a->key_length_len != 1 && a->key_length_len != a->N))
+        a->Bp < 0 || (a->key_length_len != 1 && a->key_length_len != a->N))
         return KVR_ERR_SHAPE;
     if (rope && (a->Dr < 2 || (a->Dr & 1) || a->Dr > a->Di)) return KVR_ERR_SHAPE;
     if (!(a->eps >= 0.f)) return KVR_ERR_SHAPE;
-    if (a->N * a->L == 0) return KVR_OK;
-    if (a->raw_index_keys == nullptr || a->block_keys == nullptr || a->key_length == nullptr ||
+    // Concat-output form: the past block keys come from a separate buffer.
+    const bool concat = a->past_block_index_keys != nullptr && a->past_block_index_keys != a->block_keys;
+    // Without new tokens only the carry outputs and the past-row copy remain.
+    if (a->N == 0 ||
+        (a->L == 0 && !concat && a->next_incomplete_raw_keys == nullptr && a->next_incomplete_rope == nullptr))
+        return KVR_OK;
+    if ((a->L > 0 && a->raw_index_keys == nullptr) || a->block_keys == nullptr || a->key_length == nullptr ||
         a->past_incomplete_raw_keys == nullptr)
         return KVR_ERR_NULL;
-    if (rope && (a->rope_cos == nullptr || a->rope_sin == nullptr || a->past_incomplete_rope == nullptr))
-        return KVR_ERR_NULL;
+    if (rope && a->past_incomplete_rope == nullptr) return KVR_ERR_NULL;
+    if (rope && a->L > 0 && (a->rope_cos == nullptr || a->rope_sin == nullptr)) return KVR_ERR_NULL;
     if (!rope && a->past_incomplete_rope != nullptr) return KVR_ERR_NULL;
     if (!rope && a->next_incomplete_rope != nullptr) return KVR_ERR_NULL;
-    const int64_t nbmax = (a->L + a->key_block_size - 1) / a->key_block_size;
-    if (a->N * (nbmax + 1) > 0x7FFFFFFFLL) return KVR_ERR_SHAPE;
+    const int64_t kbs = a->key_block_size;
+    const int64_t nbmax = (a->L + kbs - 1) / kbs;
+    // Past rows copied per CTA in the concat form: about 16 KB.
+    const int64_t copy_rows = a->Di * 2 >= 16384 ? 1 : 16384 / (a->Di * 2);
+    const int64_t ncopy = concat ? (std::min(a->Bp, a->Bcap) + copy_rows - 1) / copy_rows : 0;
+    if (a->N * (nbmax + 1 + ncopy) > 0x7FFFFFFFLL) return KVR_ERR_SHAPE;
     const void* ptrs[] = {a->raw_index_keys, a->block_keys, a->rope_cos, a->rope_sin, a->k_norm_weight,
                           a->past_incomplete_raw_keys, a->past_incomplete_rope, a->next_incomplete_raw_keys,
-                          a->next_incomplete_rope};
+                          a->next_incomplete_rope, a->past_block_index_keys};
     for (const void* q : ptrs)
         if (!aligned(q, 2)) return KVR_ERR_SHAPE;
     if (!aligned(a->key_length, 8)) return KVR_ERR_SHAPE;
 
     const int64_t Dr = rope ? a->Dr : 0;
-    const int64_t kbs = a->key_block_size;
     const int64_t nr_bytes = a->N * (kbs - 1) * a->Di * 2;
     const int64_t nrope_bytes = a->N * 2 * Dr * 2;
     const void* ins[] = {a->raw_index_keys, a->block_keys, a->rope_cos, a->rope_sin, a->k_norm_weight,
-                         a->past_incomplete_raw_keys, a->past_incomplete_rope, a->key_length};
+                         a->past_incomplete_raw_keys, a->past_incomplete_rope, a->key_length,
+                         concat ? a->past_block_index_keys : nullptr};
     const int64_t in_bytes[] = {a->N * a->L * a->Di * 2, a->N * a->Bcap * a->Di * 2, a->N * a->L * Dr * 2,
-                                a->N * a->L * Dr * 2, a->Di * 2, nr_bytes, nrope_bytes, a->key_length_len * 8};
-    for (int i = 0; i < 8; ++i)
+                                a->N * a->L * Dr * 2, a->Di * 2, nr_bytes, nrope_bytes, a->key_length_len * 8,
+                                a->N * a->Bp * a->Di * 2};
+    constexpr int n_ins = sizeof(ins) / sizeof(ins[0]);
+    for (int i = 0; i < n_ins; ++i)
         if (overlap(a->next_incomplete_raw_keys, nr_bytes, ins[i], in_bytes[i]) ||
             overlap(a->next_incomplete_rope, nrope_bytes, ins[i], in_bytes[i]))
             return KVR_ERR_ALIAS;
     if (overlap(a->next_incomplete_raw_keys, nr_bytes, a->next_incomplete_rope, nrope_bytes)) return KVR_ERR_ALIAS;
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < n_ins; ++i)
         if (i != 1 && overlap(a->block_keys, in_bytes[1], ins[i], in_bytes[i])) return KVR_ERR_ALIAS;
 
     QsaParams p;
@@ -240,15 +258,22 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
     p.past_rope = a->past_incomplete_rope;
     p.next_raw = a->next_incomplete_raw_keys;
     p.next_rope = a->next_incomplete_rope;
+    p.past_bk = concat ? a->past_block_index_keys : nullptr;
     p.status = a->dev_status;
     p.N = a->N;
     p.L = a->L;
     p.Bcap = a->Bcap;
     p.kbs = kbs;
     p.nbmax = nbmax;
+    p.Bp = a->Bp;
+    p.ncopy = ncopy;
+    p.copy_rows = int(copy_rows);
+    p.copy_vec = concat && a->Di % 8 == 0 && aligned(a->past_block_index_keys, 16) && aligned(a->block_keys, 16);
     p.key_length_per_seq = a->key_length_len == a->N && a->N > 1;
     p.Di = int(a->Di);
     p.Dr = int(Dr);
+    p.rope_first = a->rope_layout == KVR_QSA_ROPE_INTERLEAVE_FIRST || a->rope_layout == KVR_QSA_ROPE_HALF_FIRST;
+    p.rope_half = a->rope_layout == KVR_QSA_ROPE_HALF_LAST || a->rope_layout == KVR_QSA_ROPE_HALF_FIRST;
     p.eps = a->eps;
     p.inv_di = 1.0f / float(a->Di);
     p.inv_kbs = 1.0f / float(kbs);

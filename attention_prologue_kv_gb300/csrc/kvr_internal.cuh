@@ -261,11 +261,18 @@ struct QsaParams {
     const void* past_rope;
     void* next_raw;
     void* next_rope;
+    const void* past_bk;  // concat-output form: past block keys [N, Bp, Di], else NULL
     int32_t* status;
     int64_t N, L, Bcap, kbs;
     int64_t nbmax;       // CTAs per sequence for block keys = ceil(L / kbs)
+    int64_t Bp;          // rows of past_bk per sequence
+    int64_t ncopy;       // CTAs per sequence copying past rows (0 unless past_bk)
+    int copy_rows;       // past rows per copy CTA
+    int copy_vec;        // the copy may use 16-byte accesses
     int key_length_per_seq;
     int Di, Dr;
+    int rope_first;      // rotate channels [0, Dr) instead of [Di-Dr, Di)
+    int rope_half;       // rotate-half pairs (x[i], x[i+Dr/2]) instead of (x[2i], x[2i+1])
     float eps, inv_di, inv_kbs;
 };
 

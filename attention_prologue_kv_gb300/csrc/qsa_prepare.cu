@@ -6,8 +6,10 @@
 // first token; past tokens of the incomplete block come from the carried
 // past_incomplete_raw_keys / past_incomplete_rope. The normalisation and the
 // rotation are the rmsNorm / interleaveRope formulas of
-// "aclnnKvRmsNormRopeCache" ("Formulas (1)", "Formulas (2)"), the rotation on
-// the last Dr channels.
+// "aclnnKvRmsNormRopeCache" ("Formulas (1)", "Formulas (2)"), the rotation by
+// default on the last Dr channels with interleaved pairs (the first Dr
+// channels and rotate-half pairs on request). In the concat-output form the
+// past block keys are copied from past_block_index_keys first.
 //
 // Design: one CTA per (sequence, candidate block), 256 threads; the CTA
 // reads key_length on the device, derives the past length P = K - L, and
@@ -17,7 +19,8 @@
 // float32, and the G partial rows are reduced in shared memory. The mean,
 // the block-wide sum of squares, the rotation and one rounding to the
 // output type follow; the 2*Di-byte key row is written once. One extra CTA
-// per sequence writes the optional carry outputs.
+// per sequence writes the optional carry outputs, and in the concat-output
+// form `ncopy` more CTAs per sequence copy its past block-key rows.
 #include <mutex>
 #include <set>
 
@@ -41,6 +44,44 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return red[QSA_THREADS / 32];
 }
 
+// Lanes (within the rotated channels) of pair member a and b for output lane
+// i in [0, Dr): pair q = i mod Dr/2 is (2q, 2q+1) interleaved or (q, q+Dr/2)
+// rotate-half; lane i < Dr/2 takes a*cos - b*sin, the rest b*cos + a*sin.
+__device__ __forceinline__ void rope_pair_lanes(int i, int h, int half, int& la, int& lb) {
+    const int q = i < h ? i : i - h;
+    la = half ? q : 2 * q;
+    lb = half ? q + h : 2 * q + 1;
+}
+
+// Concat-output form: copy CTA `c` of sequence n copies past block-key rows
+// [c*copy_rows, (c+1)*copy_rows) below min(Bp, floor(P/kbs), Bcap).
+__device__ __forceinline__ void copy_past_block_keys(const QsaParams& p, int64_t n, int64_t c, int64_t j0,
+                                                     int tid, int nthreads) {
+    const int64_t lim = min(min(p.Bp, j0), p.Bcap);
+    const int64_t r0 = c * p.copy_rows;
+    const int64_t r1 = min(r0 + int64_t(p.copy_rows), lim);
+    if (r1 <= r0) return;
+    const int64_t row_b = int64_t(p.Di) * 2;
+    const char* src = static_cast<const char*>(p.past_bk) + (n * p.Bp + r0) * row_b;
+    char* dst = static_cast<char*>(p.block_keys) + (n * p.Bcap + r0) * row_b;
+    const int64_t bytes = (r1 - r0) * row_b;
+    if (p.copy_vec) {
+#pragma unroll 4
+        for (int64_t e = tid; e < (bytes >> 4); e += nthreads)
+            reinterpret_cast<uint4*>(dst)[e] = ld_stream_v4(src + 16 * e);
+    } else {
+        for (int64_t e = tid; e < (bytes >> 1); e += nthreads)
+            reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
+    }
+}
+
+// Status bits of the concat-output form for sequence n (one thread).
+__device__ __forceinline__ void past_block_status(const QsaParams& p, int64_t j0) {
+    if (p.past_bk == nullptr || p.status == nullptr) return;
+    if (p.Bp < j0) atomicOr(p.status, KVR_DEVERR_PAST_BLOCKS);
+    if (min(p.Bp, j0) > p.Bcap) atomicOr(p.status, KVR_DEVERR_BLOCK_CAP);
+}
+
 template <class IT, int VW>
 __device__ __forceinline__ void accumulate(const uint16_t* src, float* acc) {
     if constexpr (VW == 8) {
@@ -60,7 +101,7 @@ template <class IT, int VW>
 __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
     extern __shared__ __align__(16) float sm[];
     const int tid = threadIdx.x;
-    const int64_t per_seq = p.nbmax + 1;
+    const int64_t per_seq = p.nbmax + 1 + p.ncopy;
     const int64_t n = int64_t(blockIdx.x) / per_seq;
     const int64_t jl = int64_t(blockIdx.x) - n * per_seq;
 
@@ -80,7 +121,12 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
     const uint16_t* raw = static_cast<const uint16_t*>(p.raw) + n * p.L * Di;
     const uint16_t* past = static_cast<const uint16_t*>(p.past_raw) + n * (kbs - 1) * Di;
 
+    if (jl > p.nbmax) {
+        copy_past_block_keys(p, n, jl - p.nbmax - 1, j0, tid, QSA_THREADS);
+        return;
+    }
     if (jl == p.nbmax) {
+        if (tid == 0) past_block_status(p, j0);
         // ---- carry outputs: tokens after the last completed block ----
         const int64_t Fn = (K / kbs) * kbs;
         const int64_t rem = K - Fn;
@@ -158,7 +204,7 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
     }
     __syncthreads();
 
-    // ---- rotation of the last Dr channels with the first token's RoPE, write ----
+    // ---- rotation with the first token's RoPE, write ----
     const uint16_t* cr = nullptr;
     const uint16_t* sr = nullptr;
     if (p.Dr > 0) {
@@ -170,18 +216,19 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
             sr = cr + p.Dr;
         }
     }
-    const int base = Di - p.Dr;
+    const int base = p.rope_first ? 0 : Di - p.Dr;
     const int h = p.Dr >> 1;
     uint16_t* out = static_cast<uint16_t*>(p.block_keys) + (n * p.Bcap + j) * Di;
     for (int ch = tid; ch < Di; ch += QSA_THREADS) {
         float v;
-        if (ch < base) {
+        const int i = ch - base;                  // table lane in [0, Dr) when rotated
+        if (unsigned(i) >= unsigned(p.Dr)) {
             v = u[ch];
         } else {
-            const int i = ch - base;              // table lane in [0, Dr)
-            const int q = i < h ? i : i - h;      // pair index
-            const float a = u[base + 2 * q];      // x1 = even lane
-            const float b = u[base + 2 * q + 1];  // x2 = odd lane
+            int la, lb;
+            rope_pair_lanes(i, h, p.rope_half, la, lb);
+            const float a = u[base + la];
+            const float b = u[base + lb];
             const float c = IT::one(cr[i]);
             const float s = IT::one(sr[i]);
             v = i < h ? a * c - b * s : b * c + a * s;
@@ -199,6 +246,9 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 // of shared memory.
 // ---------------------------------------------------------------------------
 
+#ifndef KVR_QSA_RAW_PREFETCH
+#define KVR_QSA_RAW_PREFETCH 1
+#endif
 #ifndef KVR_QSA_BULK_THREADS
 #define KVR_QSA_BULK_THREADS 128
 #endif
@@ -222,7 +272,7 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
 
     // This CTA's candidate (sequence n, local block jl); 32-bit: the grid has
     // fewer than 2^31 CTAs.
-    const uint32_t per_seq = uint32_t(p.nbmax + 1);
+    const uint32_t per_seq = uint32_t(p.nbmax + 1 + p.ncopy);
     const uint32_t n32 = blockIdx.x / per_seq;
     const int64_t n = n32;
     const int64_t jl = int64_t(blockIdx.x - n32 * per_seq);
@@ -232,6 +282,18 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
+#if KVR_QSA_RAW_PREFETCH
+        // New-key rows [jl*kbs, (jl+1)*kbs) on their way into L2 while
+        // key_length is read: the block this CTA computes starts P mod kbs
+        // rows earlier, but the union over the sequence's CTAs covers every
+        // row a completed block reads. (A prefetch is only a hint; L2 is the
+        // coherence point, so it is safe before the dependency wait.)
+        if (jl < p.nbmax) {
+            const int64_t r0 = jl * kbs;
+            const int64_t nr = min(kbs, p.L - r0);
+            prefetch_l2_bulk(static_cast<const uint16_t*>(p.raw) + (n * p.L + r0) * Di, uint32_t(nr * Di * 2));
+        }
+#endif
     }
     pdl_wait();
     pdl_launch_dependents();
@@ -259,7 +321,12 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     const uint16_t* raw = static_cast<const uint16_t*>(p.raw) + n * p.L * Di;
     const uint16_t* past = static_cast<const uint16_t*>(p.past_raw) + n * (kbs - 1) * Di;
 
+    if (jl > p.nbmax) {
+        copy_past_block_keys(p, n, jl - p.nbmax - 1, j0, tid, QSA_BULK_THREADS);
+        return;
+    }
     if (jl == p.nbmax) {
+        if (tid == 0) past_block_status(p, j0);
         // carry outputs (small; plain loads and stores)
         const int64_t Fn = (j0 + nb) * kbs;
         const int rem = int(K - Fn);
@@ -377,19 +444,20 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     }
     __syncthreads();
 
-    // ---- rotation of the last Dr channels, one rounding, write the key row ----
-    const int base = Di - p.Dr;
+    // ---- rotation of the layout's Dr channels, one rounding, write the key row ----
+    const int base = p.rope_first ? 0 : Di - p.Dr;
     const int h = p.Dr >> 1;
     uint16_t* out = static_cast<uint16_t*>(p.block_keys) + (n * p.Bcap + j) * Di;
     for (int ch = tid; ch < Di; ch += QSA_BULK_THREADS) {
         float v;
-        if (ch < base) {
+        const int i = ch - base;
+        if (unsigned(i) >= unsigned(p.Dr)) {
             v = u[ch];
         } else {
-            const int i = ch - base;
-            const int q = i < h ? i : i - h;
-            const float a = u[base + 2 * q];
-            const float b = u[base + 2 * q + 1];
+            int la, lb;
+            rope_pair_lanes(i, h, p.rope_half, la, lb);
+            const float a = u[base + la];
+            const float b = u[base + lb];
             const float c = IT::one(rope_s[i]);
             const float s = IT::one(rope_s[p.Dr + i]);
             v = i < h ? a * c - b * s : b * c + a * s;
@@ -408,7 +476,7 @@ static size_t qsa_bulk_smem(const QsaParams& p) {
 }
 
 cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, cudaStream_t s) {
-    const int64_t grid = p.N * (p.nbmax + 1);
+    const int64_t grid = p.N * (p.nbmax + 1 + p.ncopy);
     const size_t bsmem = bulk ? qsa_bulk_smem(p) : 0;
     if (bsmem > 0) {
         auto fn = in_dtype == KVR_BF16 ? qsa_bulk_kernel<BF16> : qsa_bulk_kernel<F16>;

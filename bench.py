@@ -564,6 +564,33 @@ def run_extras(dev, kvr, wl, flush_buf):
     r["sets"] = "%d input sets" % len(qs)
     out["qsa_prepare"] = r
 
+    # the same sets with the other RoPE layout family, and in the concat-output
+    # form (past block keys [N, Bp, Di] copied into a fresh output first)
+    Bp = int(max(max(p_ // q.kbs for p_ in q.meta["past"]) for q in qs))
+    past_bk = torch.zeros(q0.N, Bp, q0.Di, dtype=torch.bfloat16, device=dev)
+    for name, kw, extra in (
+            ("qsa_prepare_half_first", dict(rope_layout="half_first"), lambda q: 0),
+            ("qsa_prepare_concat", dict(past_block_index_keys=past_bk),
+             lambda q: 2 * q.Di * 2 * sum(min(Bp, p_ // q.kbs) for p_ in q.meta["past"]))):
+        calls = []
+        for q in qs:
+            a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
+                 d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
+            calls.append(lambda a=a, kw=kw: kvr.qsa_prepare(*a, **kw))
+        for f in calls:
+            f()
+        iso, _ = time_each(calls[0], 20, flush, stream)
+        steady = time_graph(calls, 8 * len(calls), stream)
+        extra_mean = sum(extra(q) for q in qs) / len(qs)   # copied rows differ between sets
+        nbytes = qsa_algorithmic_bytes(nb, q0.N, q0.kbs, q0.Di, q0.Dr) + extra_mean
+        r = summary(iso * 1e3, steady * 1e3, nbytes, q0.N * q0.L, "new_tokens")
+        r["blocks"] = nb
+        r["sets"] = "%d input sets" % len(qs)
+        if name == "qsa_prepare_concat":
+            r["past_rows_copied_mean"] = extra_mean / (2 * q0.Di * 2)
+        out[name] = r
+    del past_bk
+
     # DynamicQuant of q^N for one decode step (256 tokens x 128 heads x 512)
     qs = [wl.dynamic_quant_decode(seed=1006 + 7919 * i) for i in range(nsets(256 * 128 * 512 * 2))]
     rows, H = qs[0].numel() // qs[0].shape[-1], qs[0].shape[-1]

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 1
+#define KVR_ABI_VERSION 2
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -78,6 +78,8 @@ typedef enum kvr_status {
 #define KVR_DEVERR_BLOCK_CAP 0x4   /* qsa: a completed block's number is >= Bcap */
 #define KVR_DEVERR_TIMEOUT 0x8     /* a pipeline wait inside a kernel exceeded its limit
                                       (one second); that CTA stopped early, output incomplete */
+#define KVR_DEVERR_PAST_BLOCKS 0x10 /* qsa, concat-output form: past_block_index_keys holds
+                                      fewer than floor(P/kbs) rows for a sequence */
 
 typedef enum kvr_dtype {
     KVR_BF16 = 0,
@@ -158,6 +160,17 @@ typedef struct kvr_kv_args {
 
 kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);
 
+/* Which Dr channels the QSA rotation acts on and how it pairs them (the
+ * qsa_prepare page names neither). Every layout writes pair i's results to
+ * lanes i and i + Dr/2 of the rotated channels with cos/sin lanes i and
+ * i + Dr/2, as the interleaved RoPE of "aclnnKvRmsNormRopeCache" does. */
+typedef enum kvr_qsa_rope {
+    KVR_QSA_ROPE_INTERLEAVE_LAST = 0,   /* pairs (x[2i], x[2i+1]) of channels [Di-Dr, Di) */
+    KVR_QSA_ROPE_INTERLEAVE_FIRST = 1,  /* the same pairs of channels [0, Dr) */
+    KVR_QSA_ROPE_HALF_LAST = 2,         /* rotate-half pairs (x[i], x[i+Dr/2]) of [Di-Dr, Di) */
+    KVR_QSA_ROPE_HALF_FIRST = 3         /* rotate-half pairs of [0, Dr) */
+} kvr_qsa_rope;
+
 /*
  * Arguments of qsa_prepare(). Inputs follow the parameter list of
  * "openvino.opset17.qsa_prepare".
@@ -167,13 +180,16 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);
  *                   earlier calls (past_block_index_keys) followed by room for
  *                   new ones. Block j (tokens [j*kbs, (j+1)*kbs) of the
  *                   sequence) is written at row j; no other row is touched.
+ *                   In the concat-output form (below) rows j < floor(P/kbs)
+ *                   are first copied from past_block_index_keys.
  *   key_length      int64 [N] or [1] (key_length_len = N or 1): valid key
  *                   tokens of each sequence AFTER this call, so the past
  *                   length is P = key_length - L (< 0: KVR_DEVERR_KEY_LENGTH,
  *                   the sequence is skipped). A [1] value applies to all N.
  *   rope_cos, rope_sin  [N, L, Dr] RoPE of every new token, or both NULL to
- *                   disable the rotation. The rotation is the interleaved RoPE
- *                   of "aclnnKvRmsNormRopeCache" on channels [Di-Dr, Di).
+ *                   disable the rotation. By default the rotation is the
+ *                   interleaved RoPE of "aclnnKvRmsNormRopeCache" on channels
+ *                   [Di-Dr, Di); rope_layout selects another (kvr_qsa_rope).
  *   k_norm_weight   [Di] or NULL (NULL disables the RMS normalisation).
  *   past_incomplete_raw_keys  [N, kbs-1, Di]: raw keys of the past tokens of
  *                   the incomplete block (rows >= P mod kbs are never read).
@@ -189,9 +205,19 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);
  *                   The next_* outputs must not overlap any input
  *                   (KVR_ERR_ALIAS), so two carry buffers alternate between calls.
  *   dev_status      optional int32 device word (KVR_DEVERR_KEY_LENGTH,
- *                   KVR_DEVERR_BLOCK_CAP).
+ *                   KVR_DEVERR_BLOCK_CAP, KVR_DEVERR_PAST_BLOCKS).
+ *   rope_layout     kvr_qsa_rope (0, the default, keeps the reading above).
+ *   past_block_index_keys, Bp  concat-output form: [N, Bp, Di] `in_dtype`,
+ *                   the page's past_block_index_keys as a separate input.
+ *                   NULL (or equal to block_keys) = in place: block_keys
+ *                   already holds them. Otherwise rows j < min(Bp,
+ *                   floor(P/kbs)) are copied to block_keys (past rows at or
+ *                   beyond Bcap: KVR_DEVERR_BLOCK_CAP; Bp < floor(P/kbs):
+ *                   KVR_DEVERR_PAST_BLOCKS, the missing rows stay untouched),
+ *                   so block_keys ends as the past keys followed by the new
+ *                   ones. It must not overlap block_keys or the next_* outputs.
  *
- * Limits: N, L >= 0; Di >= 1; 0 <= Dr <= Di, Dr even; Bcap >= 1.
+ * Limits: N, L >= 0; Di >= 1; 0 <= Dr <= Di, Dr even; Bcap >= 1; Bp >= 0.
  * Mean, normalisation and rotation in float32, one rounding to `in_dtype`.
  */
 typedef struct kvr_qsa_args {
@@ -213,6 +239,9 @@ typedef struct kvr_qsa_args {
     void* next_incomplete_raw_keys;
     void* next_incomplete_rope;
     int32_t* dev_status;
+    kvr_qsa_rope rope_layout;
+    const void* past_block_index_keys;
+    int64_t Bp;
 } kvr_qsa_args;
 
 kvr_status qsa_prepare(const kvr_qsa_args* args, cudaStream_t stream);

@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.kvr_abi_version() == 1
+    assert lib.kvr_abi_version() == N.ABI_VERSION == 2
 
 
 def test_status_strings(lib):
@@ -157,6 +157,13 @@ def _qsa_args(**kw):
     (dict(next_incomplete_raw_keys=(1 << 20) * 48), N.KVR_ERR_ALIAS),
     (dict(next_incomplete_rope=(1 << 20) * 56 + 2), N.KVR_ERR_ALIAS),
     (dict(block_keys=(1 << 20) + 64), N.KVR_ERR_ALIAS),
+    (dict(rope_layout=4), N.KVR_ERR_MODE),
+    (dict(rope_layout=-1), N.KVR_ERR_MODE),
+    (dict(Bp=-1), N.KVR_ERR_SHAPE),
+    (dict(past_block_index_keys=(1 << 20) * 8 + 256, Bp=4), N.KVR_ERR_ALIAS),     # overlaps block_keys
+    (dict(past_block_index_keys=(1 << 20) * 64, Bp=4,
+          next_incomplete_raw_keys=(1 << 20) * 64 + 32), N.KVR_ERR_ALIAS),       # carry out over it
+    (dict(past_block_index_keys=(1 << 20) * 64 + 1, Bp=4), N.KVR_ERR_SHAPE),     # misaligned
 ])
 def test_qsa_host_validation(lib, kw, want):
     a = _qsa_args(**kw)
@@ -164,7 +171,12 @@ def test_qsa_host_validation(lib, kw, want):
 
 
 def test_qsa_empty_problem_is_ok(lib):
+    """No new tokens and nothing else to write: OK without a launch (the
+    token tables may then be NULL). With carry outputs or a separate past
+    buffer an L = 0 call still has work, so it is not returned early."""
     assert lib.qsa_prepare(ctypes.byref(_qsa_args(L=0)), None) == N.KVR_OK
+    assert lib.qsa_prepare(ctypes.byref(_qsa_args(L=0, raw_index_keys=None, rope_cos=None,
+                                                  rope_sin=None)), None) == N.KVR_OK
     assert lib.qsa_prepare(ctypes.byref(_qsa_args(N=0, key_length_len=0)), None) in (N.KVR_OK, N.KVR_ERR_SHAPE)
 
 

@@ -12,10 +12,16 @@ from helpers import compare_cache, run_gpu_qsa, run_oracle_qsa
 pytestmark = pytest.mark.gpu
 
 
-def check(case, carry=True):
-    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, carry=carry)
-    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, carry=carry)
+def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None):
+    kw = dict(carry=carry, rope_layout=rope_layout, past_block_keys=past_block_keys)
+    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, **kw)
     assert g_st == r_st
+    if past_block_keys is not None:
+        # copied past rows are bit-exact copies
+        for n, P in enumerate(case.meta["past"]):
+            m = min(past_block_keys.shape[1], P // case.kbs, case.Bcap)
+            assert np.array_equal(g_bk[n, :m], r_bk[n, :m])
     n, exact = compare_cache(g_bk, r_bk, "bf16", case.Di)
     if carry:
         assert np.array_equal(g_nr, r_nr, equal_nan=True)
@@ -99,3 +105,103 @@ def test_pipeline_ring_depths(N, L, Di, Dr, kbs):
     case = wl.make_qsa_case("r", N, L, Di=Di, Dr=Dr, kbs=kbs, seed=N + L, past_max=500)
     n, _ = check(case)
     assert n == case.completed_blocks()
+
+
+# ---- RoPE layouts on each kernel variant: bulk copies (Di, Dr multiples of
+# 8), register loads (Dr not a multiple of 8), scalar loads (Di odd multiple of 4) ----
+
+@pytest.mark.parametrize("layout", ["interleave_last", "interleave_first", "half_last", "half_first"])
+@pytest.mark.parametrize("Di,Dr,kbs", [(128, 64, 64), (24, 6, 5), (12, 4, 3), (16, 16, 2)])
+def test_rope_layouts(layout, Di, Dr, kbs):
+    case = wl.make_qsa_case("l", 5, 37, Di=Di, Dr=Dr, kbs=kbs, seed=Di * 3 + kbs, past_max=300)
+    n, _ = check(case, rope_layout=layout)
+    assert n == case.completed_blocks()
+
+
+def test_rope_layout_full_size_half_first():
+    case = wl.qsa_prepare_workload()
+    n, exact = check(case, rope_layout="half_first")
+    assert n == case.completed_blocks() and exact > 0.97
+
+
+# ---- concat-output form ----
+
+def _past_codes(case, Bp, seed):
+    return np.random.default_rng(seed).integers(0, 0x7F00, (case.N, Bp, case.Di), dtype=np.uint16)
+
+
+def test_concat_form_full_size():
+    case = wl.qsa_prepare_workload()
+    P = np.array(case.meta["past"])
+    past = _past_codes(case, int((P // case.kbs).max()), 31)
+    n, exact = check(case, past_block_keys=past)
+    assert n == case.completed_blocks() + int((P // case.kbs).sum())
+
+
+@pytest.mark.parametrize("Di,Dr,kbs", [(128, 64, 4), (24, 8, 3), (12, 4, 2), (8192 // 2, 64, 2)])
+def test_concat_form_shapes(Di, Dr, kbs):
+    """Several copy CTAs per sequence (Di = 128, 4096: 64 rows and 2 rows per
+    CTA), the 16-byte and the 2-byte copy."""
+    case = wl.make_qsa_case("c", 4, 21, Di=Di, Dr=Dr, kbs=kbs, seed=Di + kbs, past_max=400)
+    P = np.array(case.meta["past"])
+    past = _past_codes(case, int((P // kbs).max()) + 3, Di)
+    check(case, past_block_keys=past)
+
+
+def test_concat_form_status_bits():
+    # sequence 1: 5 past blocks but a 3-row past buffer; sequence 2: past rows beyond Bcap
+    case = wl.make_qsa_case("s", 3, 4, Di=16, Dr=8, kbs=4, seed=32, past=[4, 20, 40], Bcap=9)
+    past = _past_codes(case, 3, 33)
+    assert run_oracle_qsa(case, past_block_keys=past)[3] == 0x10 | 0x4
+    check(case, past_block_keys=past)
+    case2 = wl.make_qsa_case("s", 1, 4, Di=16, Dr=8, kbs=4, seed=34, past=[40], Bcap=6)
+    past2 = _past_codes(case2, 12, 35)
+    assert run_oracle_qsa(case2, past_block_keys=past2)[3] == 0x4
+    check(case2, past_block_keys=past2)
+
+
+def test_concat_form_same_buffer_is_in_place():
+    import attention_prologue_kv_gb300 as kvr
+    case = wl.make_qsa_case("i", 3, 20, Di=32, Dr=8, kbs=4, seed=36, past=[0, 6, 13])
+    ref, _, _, _ = run_gpu_qsa(case)
+    dev = "cuda"
+    bk = torch.full((case.N, case.Bcap, case.Di), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    d = lambda t: t.to(dev)
+    kvr.qsa_prepare(d(case.raw), bk, d(case.key_length), d(case.rope_cos), d(case.rope_sin),
+                    d(case.k_norm_weight), d(case.past_raw), d(case.past_rope), case.kbs, case.eps,
+                    past_block_index_keys=bk)
+    torch.cuda.synchronize()
+    assert np.array_equal(bk.cpu().view(torch.int16).numpy(), ref.view(np.int16))
+
+
+def test_no_new_tokens_still_writes_carry_and_past_rows():
+    """L = 0: no block completes, but the carry outputs pass the carried keys
+    on and the concat form still copies the past rows."""
+    case = wl.make_qsa_case("z", 3, 0, Di=32, Dr=8, kbs=4, seed=37, past=[5, 8, 14])
+    P = np.array(case.meta["past"])
+    n, _ = check(case, carry=True, past_block_keys=_past_codes(case, 4, 38))
+    assert n == int(np.minimum(P // 4, 4).sum())
+
+
+def test_chained_concat_calls_equal_one_call():
+    """Each call writes a fresh buffer from the previous one (concat form);
+    the last equals one in-place call over all tokens."""
+    import attention_prologue_kv_gb300 as kvr
+    N, L, Di, Dr, kbs = 3, 40, 32, 8, 6
+    case = wl.make_qsa_case("t", N, L, Di=Di, Dr=Dr, kbs=kbs, seed=39, past=[0, 5, 13], Bcap=12)
+    whole, _, _, _ = run_gpu_qsa(case, carry=False)
+    dev = "cuda"
+    P = torch.tensor(case.meta["past"])
+    prev = torch.full((N, 12, Di), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    past_raw, past_rope = case.past_raw.to(dev), case.past_rope.to(dev)
+    for a, b in [(0, 9), (9, 25), (25, L)]:
+        out = torch.full((N, 12, Di), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        nr = torch.full((N, kbs - 1, Di), float("nan"), dtype=torch.bfloat16, device=dev)
+        npr = torch.full((N, 2 * Dr), float("nan"), dtype=torch.bfloat16, device=dev)
+        kvr.qsa_prepare(case.raw[:, a:b].contiguous().to(dev), out, (P + b).to(dev),
+                        case.rope_cos[:, a:b].contiguous().to(dev), case.rope_sin[:, a:b].contiguous().to(dev),
+                        case.k_norm_weight.to(dev), past_raw, past_rope, kbs, case.eps,
+                        next_incomplete_raw_keys=nr, next_incomplete_rope=npr, past_block_index_keys=prev)
+        prev, past_raw, past_rope = out, nr, npr
+    torch.cuda.synchronize()
+    assert np.array_equal(prev.cpu().view(torch.int16).numpy(), whole.view(np.int16))
