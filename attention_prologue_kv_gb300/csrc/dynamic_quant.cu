@@ -41,9 +41,8 @@ __device__ __forceinline__ int dq_code(float x, float s) {
 // most 127 in magnitude, ulp(q0) <= 2^-17 there). Rounding q0 or fl32(x/s)
 // to an integer can therefore differ only when q0 lies within that distance
 // of a half-integer. With d = q0 - rint(q0) (|d| <= 1/2), the distance to the
-// nearest half-integer is 1/2 - |d|: `maxd` tracks the largest |d|, and the
-// caller recomputes the lane's codes by IEEE division when it reaches
-// 1/2 - 2^-15.
+// nearest half-integer is 1/2 - |d|: `maxd` tracks the largest |d|, and when
+// it reaches 1/2 - 2^-15 the caller repairs those elements (dq_fix_near_ties).
 // Valid while 1/s is a normal float (the caller checks s >= 2^-100).
 // Rounding: with M = 1.5 * 2^23, t = fl(q0 + M) rounds q0 (|q0| < 2^22) to an
 // integer with ties to even inside the addition, and the low byte of t's bits
@@ -78,6 +77,29 @@ __device__ __forceinline__ uint2 dq_chunk_exact(const uint4& x, float s) {
         b[2 * k + 1] = uint32_t(dq_code(IT::hi(w[k]), s)) & 0xFFu;
     }
     return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+// Repair the codes of dq_chunk_fast where the product lies within 2^-15 of a
+// half-integer: each such element (the same RN(x*y) and test as the fast
+// path) takes the IEEE division; the others keep their code. A warp runs
+// the division only at element positions where one of its lanes needs it
+// (on bfloat16 rows one element per warp on average, since q*127/m is often
+// a dyadic rational).
+template <class IT>
+__device__ __forceinline__ void dq_fix_near_ties(const uint4& x, float y, float s, uint2& o) {
+    const float T = 0.5f - 0x1p-15f;
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float v = (j & 1) ? IT::hi(w[j >> 1]) : IT::lo(w[j >> 1]);
+        const float q0 = __fmul_rn(v, y);
+        if (fabsf(__fsub_rn(q0, rintf(q0))) >= T) {
+            const uint32_t code = uint32_t(dq_code(v, s)) & 0xFFu;
+            const int sh = 8 * (j & 3);
+            if (j < 4) o.x = (o.x & ~(0xFFu << sh)) | (code << sh);
+            else o.y = (o.y & ~(0xFFu << sh)) | (code << sh);
+        }
+    }
 }
 
 // max(|a|, |b|) over the two 16-bit lanes of w, exact: clear the sign bits and
@@ -145,12 +167,11 @@ __global__ void __launch_bounds__(DQ_THREADS) dq_vec_kernel(const DqParams p) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
             if (c * 32 + lane < nch) o[c] = fast ? dq_chunk_fast<IT>(x[c], y, maxd) : dq_chunk_exact<IT>(x[c], s);
-        // Any product within 2^-15 of a half-integer: this lane's codes again,
-        // by IEEE division (rare).
+        // A product within 2^-15 of a half-integer: repair those codes.
         if (fast && !(maxd < 0.5f - 0x1p-15f)) {
 #pragma unroll
             for (int c = 0; c < CPL; ++c)
-                if (c * 32 + lane < nch) o[c] = dq_chunk_exact<IT>(x[c], s);
+                if (c * 32 + lane < nch) dq_fix_near_ties<IT>(x[c], y, s, o[c]);
         }
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
