@@ -5,7 +5,7 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvr.so")
-ABI_VERSION = 2   # KVR_ABI_VERSION of include/kvr.h these structures mirror
+ABI_VERSION = 3   # KVR_ABI_VERSION of include/kvr.h these structures mirror
 
 # kvr_status
 KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS, KVR_ERR_CUDA = range(7)
@@ -66,7 +66,7 @@ class DqArgs(ctypes.Structure):
     ]
 
 
-EXPORTS = ("kv_rmsnorm_rope_cache", "qsa_prepare", "dynamic_quant", "kvr_device_copy",
+EXPORTS = ("kv_rmsnorm_rope_cache", "kv_rmsnorm_rope_cache_staged", "qsa_prepare", "dynamic_quant", "kvr_device_copy",
            "kvr_status_string", "kvr_abi_version")
 
 _lib = None
@@ -86,6 +86,8 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     L.kv_rmsnorm_rope_cache.argtypes = [ctypes.POINTER(KvArgs), _vp]
     L.kv_rmsnorm_rope_cache.restype = _int
+    L.kv_rmsnorm_rope_cache_staged.argtypes = [ctypes.POINTER(KvArgs), _vp, _vp, _i64, _vp, _vp]
+    L.kv_rmsnorm_rope_cache_staged.restype = _int
     L.qsa_prepare.argtypes = [ctypes.POINTER(QsaArgs), _vp]
     L.qsa_prepare.restype = _int
     L.dynamic_quant.argtypes = [ctypes.POINTER(DqArgs), _vp]

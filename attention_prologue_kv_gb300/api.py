@@ -146,17 +146,45 @@ class PreparedCall:
     tensors alive and unmoved for the object's lifetime. For serving loops
     that reuse fixed buffers every step: a call costs the C entry point only."""
 
-    def __init__(self, fn, args, name, keep):
+    def __init__(self, fn, args, name, keep, staged_fn=None):
         self._fn = fn
         self._args = args
         self._ref = ctypes.byref(args)
         self._name = name
         self._keep = keep
+        self._staged_fn = staged_fn
 
     def __call__(self, stream=None):
         st = self._fn(self._ref, _stream(stream))
         if st != N.KVR_OK:
             raise KvrError(st, self._name)
+
+    def staged(self, host_src, dev_dst, nbytes, host_status=None, stream=None):
+        """The call with host staging, enqueued in one C call: copy `nbytes`
+        from pinned host memory `host_src` to device memory `dev_dst` (where
+        the bound input tensors live), run the call, then copy the device
+        status word to pinned host memory `host_status` (optional; needs
+        dev_status bound). Each of host_src, dev_dst, host_status is a tensor
+        or a raw address; raw addresses skip the checks. Asynchronous: the
+        host buffers must stay valid until the stream has passed them."""
+        if self._staged_fn is None:
+            raise TypeError("%s has no host-staged form" % self._name)
+        src = _host_addr(host_src, "host_src")
+        dst = dev_dst if isinstance(dev_dst, int) else _ptr(dev_dst, "dev_dst")
+        hst = None if host_status is None else _host_addr(host_status, "host_status")
+        st = self._staged_fn(self._ref, src, dst, int(nbytes), hst, _stream(stream))
+        if st != N.KVR_OK:
+            raise KvrError(st, self._name + "_staged")
+
+
+def _host_addr(t, name):
+    if isinstance(t, int):
+        return t
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("%s must be pinned host memory" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
 
 
 def prepare_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
@@ -166,7 +194,8 @@ def prepare_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache
     a = _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ckv_scale,
                  k_scale, kc_scale, dev_status)
     keep = (kv, gamma, cos, sin, index, ckv_cache, k_cache, ckv_scale, k_scale, dev_status)
-    return PreparedCall(N.lib().kv_rmsnorm_rope_cache, a, "kv_rmsnorm_rope_cache", keep)
+    return PreparedCall(N.lib().kv_rmsnorm_rope_cache, a, "kv_rmsnorm_rope_cache", keep,
+                        staged_fn=N.lib().kv_rmsnorm_rope_cache_staged)
 
 
 def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,

@@ -83,24 +83,20 @@ kvr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVR_OK : KVR_E
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int kvr_abi_version(void) { return KVR_ABI_VERSION; }
+// A validated kv_rmsnorm_rope_cache call, ready to launch.
+struct KvPlan {
+    KvParams p;
+    int path;
+    int in_dtype;
+    int ckv_kind;
+};
 
-const char* kvr_status_string(kvr_status s) {
-    switch (s) {
-        case KVR_OK: return "ok";
-        case KVR_ERR_NULL: return "a required pointer is NULL, or an optional pair is half given";
-        case KVR_ERR_SHAPE: return "a size is outside its documented range";
-        case KVR_ERR_DTYPE: return "an element type is not supported for that argument";
-        case KVR_ERR_MODE: return "unknown cache mode";
-        case KVR_ERR_ALIAS: return "an output overlaps an input it must not overlap";
-        case KVR_ERR_CUDA: return "the CUDA launch failed";
-    }
-    return "unknown status";
-}
-
-kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
+// Validate the arguments of kv_rmsnorm_rope_cache and fill the launch plan;
+// `*empty` is set when there is nothing to launch (T = 0).
+kvr_status kv_plan(const kvr_kv_args* a, KvPlan* plan, bool* empty) {
+    *empty = false;
     if (a == nullptr) return KVR_ERR_NULL;
     if (a->Bkv < 0 || a->Skv < 0 || a->Dv < 1 || a->Dk < 2 || (a->Dk & 1) || a->cache_d0 < 1 ||
         a->cache_d1 < 1 || a->Dv > (int64_t(1) << 30) || a->Dk > (int64_t(1) << 30))
@@ -116,7 +112,10 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
     if (a->mode == KVR_CACHE_NORM && a->cache_d0 < a->Bkv) return KVR_ERR_SHAPE;
     if (!(a->eps >= 0.f) || !(a->kc_scale == a->kc_scale)) return KVR_ERR_SHAPE;
     const int64_t T = a->Bkv * a->Skv;
-    if (T == 0) return KVR_OK;   // empty input: caches are not updated
+    if (T == 0) {   // empty input: caches are not updated
+        *empty = true;
+        return KVR_OK;
+    }
     if (a->kv == nullptr || a->gamma == nullptr || a->cos == nullptr || a->sin == nullptr ||
         a->index == nullptr || a->ckv_cache == nullptr || a->k_cache == nullptr)
         return KVR_ERR_NULL;
@@ -144,7 +143,8 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
             return KVR_ERR_ALIAS;
     if (overlap(a->ckv_cache, ckv_bytes, a->k_cache, k_bytes)) return KVR_ERR_ALIAS;
 
-    KvParams p = {};
+    KvParams& p = plan->p;
+    p = KvParams{};
     p.kv = a->kv;
     p.gamma = a->gamma;
     p.cos = a->cos;
@@ -185,8 +185,62 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
         p.kv_contig = stride == D;
         p.idx_bulk = a->mode != KVR_CACHE_PA_BLK_BSND && aligned(a->index, 16);
     }
+    plan->path = path;
+    plan->in_dtype = a->in_dtype;
+    plan->ckv_kind = out_kind(a->ckv_dtype);
+    return KVR_OK;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+int kvr_abi_version(void) { return KVR_ABI_VERSION; }
+
+const char* kvr_status_string(kvr_status s) {
+    switch (s) {
+        case KVR_OK: return "ok";
+        case KVR_ERR_NULL: return "a required pointer is NULL, or an optional pair is half given";
+        case KVR_ERR_SHAPE: return "a size is outside its documented range";
+        case KVR_ERR_DTYPE: return "an element type is not supported for that argument";
+        case KVR_ERR_MODE: return "unknown cache mode";
+        case KVR_ERR_ALIAS: return "an output overlaps an input it must not overlap";
+        case KVR_ERR_CUDA: return "the CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
+    KvPlan plan;
+    bool empty;
+    const kvr_status st = kv_plan(a, &plan, &empty);
+    if (st != KVR_OK || empty) return st;
     (void)cudaGetLastError();
-    return cuda_status(launch_kv(p, a->in_dtype, out_kind(a->ckv_dtype), path, stream));
+    return cuda_status(launch_kv(plan.p, plan.in_dtype, plan.ckv_kind, plan.path, stream));
+}
+
+kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* a, const void* host_src, void* dev_dst, int64_t bytes,
+                                        int32_t* host_status, cudaStream_t stream) {
+    if (a == nullptr) return KVR_ERR_NULL;
+    if (bytes < 0) return KVR_ERR_SHAPE;
+    if (bytes > 0 && (host_src == nullptr || dev_dst == nullptr)) return KVR_ERR_NULL;
+    if (host_status != nullptr && a->dev_status == nullptr) return KVR_ERR_NULL;
+    KvPlan plan;
+    bool empty;
+    const kvr_status st = kv_plan(a, &plan, &empty);
+    if (st != KVR_OK) return st;
+    (void)cudaGetLastError();
+    if (bytes > 0 && cudaMemcpyAsync(dev_dst, host_src, size_t(bytes), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return KVR_ERR_CUDA;
+    if (!empty) {
+        const cudaError_t e = launch_kv(plan.p, plan.in_dtype, plan.ckv_kind, plan.path, stream);
+        if (e != cudaSuccess) return KVR_ERR_CUDA;
+    }
+    if (host_status != nullptr &&
+        cudaMemcpyAsync(host_status, a->dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return KVR_ERR_CUDA;
+    return KVR_OK;
 }
 
 kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 2
+#define KVR_ABI_VERSION 3
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -159,6 +159,25 @@ typedef struct kvr_kv_args {
 } kvr_kv_args;
 
 kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);
+
+/*
+ * Host-staged form of kv_rmsnorm_rope_cache (no counterpart on the pages: a
+ * convenience for callers whose inputs are in host memory). On `stream`, in
+ * order: copy `bytes` bytes from host memory `host_src` to device memory
+ * `dev_dst` (the caller lays the step's inputs out there, so that the device
+ * pointers in *args point into it), run kv_rmsnorm_rope_cache(args), and,
+ * when `host_status` is given, copy *args->dev_status into *host_status.
+ * All asynchronous: the host values are read and written when the stream
+ * reaches the copies, so `host_src` and `host_status` should be pinned
+ * (page-locked) and stay valid until the stream passes them; the caller
+ * synchronises before reading *host_status. Arguments are validated first
+ * and nothing is enqueued on an error (as kv_rmsnorm_rope_cache; plus
+ * KVR_ERR_SHAPE for bytes < 0, KVR_ERR_NULL for a missing copy pointer or a
+ * host_status without args->dev_status). A failed enqueue returns
+ * KVR_ERR_CUDA (copies enqueued before it stay enqueued).
+ */
+kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* args, const void* host_src, void* dev_dst, int64_t bytes,
+                                        int32_t* host_status, cudaStream_t stream);
 
 /* Which Dr channels the QSA rotation acts on and how it pairs them (the
  * qsa_prepare page names neither). Every layout writes pair i's results to

@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.kvr_abi_version() == N.ABI_VERSION == 2
+    assert lib.kvr_abi_version() == N.ABI_VERSION == 3
 
 
 def test_status_strings(lib):
@@ -119,6 +119,24 @@ def _kv_args(**kw):
 def test_kv_host_validation(lib, kw, want):
     a = _kv_args(**kw)
     assert lib.kv_rmsnorm_rope_cache(ctypes.byref(a), None) == want
+
+
+@pytest.mark.parametrize("kw,call,want", [
+    (dict(), dict(bytes=-1), N.KVR_ERR_SHAPE),
+    (dict(), dict(host_src=None), N.KVR_ERR_NULL),
+    (dict(), dict(dev_dst=None), N.KVR_ERR_NULL),
+    (dict(), dict(host_status=1 << 40), N.KVR_ERR_NULL),          # status copy without dev_status
+    (dict(Dk=63), dict(), N.KVR_ERR_SHAPE),                        # the call's own validation first
+    (dict(ckv_cache=(1 << 20) + 64), dict(), N.KVR_ERR_ALIAS),
+    (dict(Bkv=0, kv=None), dict(bytes=0, host_src=None, dev_dst=None), N.KVR_OK),   # nothing to enqueue
+])
+def test_kv_staged_host_validation(lib, kw, call, want):
+    """The host-staged entry point validates everything before it enqueues a copy."""
+    a = _kv_args(**kw)
+    c = dict(host_src=1 << 41, dev_dst=1 << 20, bytes=4096, host_status=None)
+    c.update(call)
+    assert lib.kv_rmsnorm_rope_cache_staged(ctypes.byref(a), c["host_src"], c["dev_dst"], c["bytes"],
+                                            c["host_status"], None) == want
 
 
 def test_kv_empty_problem_is_ok_without_launch(lib):

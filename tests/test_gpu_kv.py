@@ -189,6 +189,51 @@ def test_prepared_call_matches_the_plain_call_and_sees_new_contents():
     compare_cache(codes_of(k), r_k, "bf16", 64)
 
 
+def test_staged_call_from_pinned_host_memory():
+    """kv_rmsnorm_rope_cache_staged: two batches staged from pinned host
+    memory into one device buffer, each followed by its call and a status
+    read-back; the caches equal the oracle's after both batches, the status
+    words arrive on the host (0 for a valid batch, the index bit for one with
+    an out-of-range slot), and a call with host tensors checks them."""
+    import attention_prologue_kv_gb300 as kvr
+    from helpers import codes_of
+    a = wl.make_kv_case("s", 4, 16, mode="PA_BSND", d0=16, d1=16, seed=62, skip=3)
+    b = wl.make_kv_case("s", 4, 16, mode="PA_BSND", d0=16, d1=16, seed=63, skip=2)
+    b.index[5] = 16 * 16 + 7     # out of range: skipped, KVR_DEVERR_INDEX
+    parts = lambda c: [c.kv.reshape(-1).view(torch.uint8), c.cos.reshape(-1).view(torch.uint8),
+                       c.sin.reshape(-1).view(torch.uint8), c.index.reshape(-1).view(torch.uint8)]
+    sizes = [t.numel() for t in parts(a)]
+    blob = sum(sizes)
+    host = torch.empty(2, blob, dtype=torch.uint8).pin_memory()
+    for r, c in enumerate((a, b)):
+        host[r] = torch.cat(parts(c))
+    stage = torch.zeros(blob, dtype=torch.uint8, device="cuda")
+    o = [0]
+    for n in sizes:
+        o.append(o[-1] + n)
+    kv = stage[o[0]:o[1]].view(torch.bfloat16).view(a.kv.shape)
+    cos = stage[o[1]:o[2]].view(torch.bfloat16).view(a.cos.shape)
+    sin = stage[o[2]:o[3]].view(torch.bfloat16).view(a.sin.shape)
+    idx = stage[o[3]:o[4]].view(torch.int64)
+    ckv = sentinel_cache((16, 16, 1, 512), "bf16")
+    k = sentinel_cache((16, 16, 1, 64), "bf16")
+    dev_status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    host_status = torch.full((2,), -1, dtype=torch.int32).pin_memory()
+    call = kvr.prepare_kv_rmsnorm_rope_cache(kv, a.gamma.cuda(), cos, sin, idx, ckv, k, cache_mode="PA_BSND",
+                                             dev_status=dev_status)
+    call.staged(host[0], stage, blob, host_status[0:1])
+    call.staged(host[1].data_ptr(), stage.data_ptr(), blob, host_status[1:2].data_ptr())
+    torch.cuda.synchronize()
+    assert host_status.tolist() == [0, 0x1]
+    b.gamma = a.gamma
+    r_ckv, r_k, _ = run_oracle_kv(a)
+    run_oracle_kv(b, r_ckv, r_k)
+    compare_cache(codes_of(ckv), r_ckv, "bf16", 512)
+    compare_cache(codes_of(k), r_k, "bf16", 64)
+    with pytest.raises(ValueError):
+        call.staged(host[0].clone(), stage, blob)          # not pinned
+
+
 def test_benchmark_decode_sets_match_the_oracle():
     """The rotating decode batches the benchmark times, through the same
     call and launch configuration, against the oracle (first four sets)."""
