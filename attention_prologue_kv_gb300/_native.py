@@ -5,7 +5,7 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvr.so")
-ABI_VERSION = 3   # KVR_ABI_VERSION of include/kvr.h these structures mirror
+ABI_VERSION = 4   # KVR_ABI_VERSION of include/kvr.h these structures mirror
 
 # kvr_status
 KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS, KVR_ERR_CUDA = range(7)
@@ -38,7 +38,7 @@ class KvArgs(ctypes.Structure):
         ("ckv_cache", _vp), ("ckv_dtype", _int), ("ckv_scale", _vp), ("ckv_scale_len", _i64),
         ("k_cache", _vp), ("k_dtype", _int), ("k_scale", _vp), ("k_scale_len", _i64),
         ("eps", _f32), ("kc_scale", _f32),
-        ("dev_status", _vp),
+        ("dev_status", _vp), ("params_ready", ctypes.c_int32),
     ]
 
 

@@ -85,7 +85,7 @@ def _cache_dims(c, name):
 
 
 def _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ckv_scale, k_scale,
-             kc_scale, dev_status):
+             kc_scale, dev_status, params_ready=False):
     _cuda(kv, "kv")
     Bkv, Skv, stride = _kv_rows(kv)
     if kv.dtype not in _IN_DTYPES:
@@ -118,12 +118,13 @@ def _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ck
         ckv_scale_len=0 if ckv_scale is None else ckv_scale.numel(),
         k_cache=k_cache.data_ptr(), k_dtype=_CACHE_DTYPES[k_cache.dtype],
         k_scale=_ptr(k_scale, "k_scale"), k_scale_len=0 if k_scale is None else k_scale.numel(),
-        eps=float(eps), kc_scale=float(kc_scale), dev_status=_ptr(dev_status, "dev_status"))
+        eps=float(eps), kc_scale=float(kc_scale), dev_status=_ptr(dev_status, "dev_status"),
+        params_ready=1 if params_ready else 0)
 
 
 def kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
                           cache_mode="PA_BSND", eps=1e-6, ckv_scale=None, k_scale=None,
-                          kc_scale=1.0, dev_status=None, stream=None):
+                          kc_scale=1.0, dev_status=None, params_ready=False, stream=None):
     """Fused RMSNorm(kv[..., :Dv]) -> ckv_cache and interleaved RoPE(kv[..., Dv:]) ->
     k_cache, scattered by `index` (-1 skips). Dv = gamma.numel().
 
@@ -131,9 +132,12 @@ def kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
     cos/sin [Bkv, 1, Skv, Dk], index int64 (layout per cache_mode),
     caches [d0, d1, 1, Dv] and [d0, d1, 1, Dk] (bf16/f16 like kv, or int8 /
     float8_e4m3fn / float8_e5m2 with a float32 scale of length D* or 1).
-    `dev_status` (int32, 1 element) collects device-side error bits."""
+    `dev_status` (int32, 1 element) collects device-side error bits.
+    params_ready=True promises that the kernel launched just before this call
+    on the stream does not write gamma or the scales (model weights and
+    calibrated scales): they are then read while that kernel still runs."""
     a = _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ckv_scale,
-                 k_scale, kc_scale, dev_status)
+                 k_scale, kc_scale, dev_status, params_ready)
     st = N.lib().kv_rmsnorm_rope_cache(ctypes.byref(a), _stream(stream))
     if st != N.KVR_OK:
         raise KvrError(st, "kv_rmsnorm_rope_cache")
@@ -189,10 +193,10 @@ def _host_addr(t, name):
 
 def prepare_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
                                   cache_mode="PA_BSND", eps=1e-6, ckv_scale=None, k_scale=None,
-                                  kc_scale=1.0, dev_status=None):
+                                  kc_scale=1.0, dev_status=None, params_ready=False):
     """kv_rmsnorm_rope_cache with its arguments bound once (see PreparedCall)."""
     a = _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ckv_scale,
-                 k_scale, kc_scale, dev_status)
+                 k_scale, kc_scale, dev_status, params_ready)
     keep = (kv, gamma, cos, sin, index, ckv_cache, k_cache, ckv_scale, k_scale, dev_status)
     return PreparedCall(N.lib().kv_rmsnorm_rope_cache, a, "kv_rmsnorm_rope_cache", keep,
                         staged_fn=N.lib().kv_rmsnorm_rope_cache_staged)

@@ -71,18 +71,22 @@ __device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane,
 //    starts as soon as its loads land (lowest latency);
 //  * otherwise gamma and the scales are staged once per CTA in shared
 //    memory, pre-widened to float (fewest instructions per row).
+// Threads per CTA of the shared-memory flavour (its CTAs stage the constants).
+#ifndef KVR_VEC_THREADS
+#define KVR_VEC_THREADS 128
+#endif
 #ifndef KVR_VEC_MIN_CTAS
-#define KVR_VEC_MIN_CTAS 8
+#define KVR_VEC_MIN_CTAS (1024 / KVR_VEC_THREADS)
 #endif
 // Small batches (the REG_GAMMA flavour) use 2-warp CTAs: the rows spread
 // over more SMs, which measured faster for a 256-row decode batch.
 template <bool REG_GAMMA>
 struct VecShape {
-    static constexpr int threads = REG_GAMMA ? 64 : KV_THREADS;
+    static constexpr int threads = REG_GAMMA ? 64 : KVR_VEC_THREADS;
     static constexpr int warps = threads / 32;
 };
 
-template <class IT, int CPL, int CK, bool REG_GAMMA>
+template <class IT, int CPL, int CK, bool REG_GAMMA, bool PARAMS_READY>
 __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : KVR_VEC_MIN_CTAS)
     kv_vec_kernel(const KvParams p) {
     constexpr int WARPS = VecShape<REG_GAMMA>::warps;
@@ -115,33 +119,40 @@ __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : 
         else if (lane == 30) prefetch_l2(static_cast<const char*>(p.sin) + t * p.Dk * 2);
         else if (lane == 31) prefetch_l2(p.index + index_pos(p, t));
     }
+    const bool cper = CK != OUT16 && p.ckv_scale_per_ch;
+    const bool kq = p.k_kind != OUT16;
+    float cscale0 = 1.f, kscale0 = 1.f;
+    uint4 graw[CPL];
+    // The launch's constants (gamma and the scales). With PARAMS_READY the
+    // caller promises that the kernel launched just before this one does not
+    // write them, so they are read before the dependency wait, overlapping
+    // that kernel; otherwise after the first row's loads are issued (staging
+    // them first would hold the row loads behind the staging stores).
+    auto load_consts = [&]() {
+        if (CK != OUT16 && !p.ckv_scale_per_ch) cscale0 = p.ckv_scale[0];
+        if (kq && !p.k_scale_per_ch) kscale0 = p.k_scale[0];
+        if constexpr (REG_GAMMA) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const int ch = c * 32 + lane;
+                if (ch < nch) graw[c] = ld_stream_v4(static_cast<const char*>(p.gamma) + ch * 16);
+            }
+        } else {
+            stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, THREADS);
+            if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, THREADS);
+            if (kq && p.k_scale_per_ch)
+                for (int i = threadIdx.x; i < p.Dk; i += THREADS) s_kscale[i] = p.k_scale[i];
+        }
+    };
+    if constexpr (PARAMS_READY) load_consts();
     pdl_wait();
     pdl_launch_dependents();
     if (REG_GAMMA && t >= p.T) return;
     RowRegs r;
     if (t < p.T) load_row<CPL>(p, t, lane, nch, h, r);
-
-    const bool cper = CK != OUT16 && p.ckv_scale_per_ch;
-    const bool kq = p.k_kind != OUT16;
-    const float cscale0 = (CK != OUT16 && !p.ckv_scale_per_ch) ? p.ckv_scale[0] : 1.f;
-    const float kscale0 = (kq && !p.k_scale_per_ch) ? p.k_scale[0] : 1.f;
-    const float* kscale = nullptr;
-    uint4 graw[CPL];
-    if constexpr (REG_GAMMA) {
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            const int ch = c * 32 + lane;
-            if (ch < nch) graw[c] = ld_stream_v4(static_cast<const char*>(p.gamma) + ch * 16);
-        }
-        kscale = (kq && p.k_scale_per_ch) ? p.k_scale : nullptr;
-    } else {
-        stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, THREADS);
-        if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, THREADS);
-        if (kq && p.k_scale_per_ch)
-            for (int i = threadIdx.x; i < p.Dk; i += THREADS) s_kscale[i] = p.k_scale[i];
-        kscale = (kq && p.k_scale_per_ch) ? s_kscale : nullptr;
-        __syncthreads();
-    }
+    if constexpr (!PARAMS_READY) load_consts();
+    const float* kscale = (kq && p.k_scale_per_ch) ? (REG_GAMMA ? p.k_scale : s_kscale) : nullptr;
+    if constexpr (!REG_GAMMA) __syncthreads();
 
     while (t < p.T) {
         const int64_t row = resolve_row(p, t, r.v);
@@ -249,21 +260,27 @@ __global__ void __launch_bounds__(KV_THREADS) kv_generic_kernel(const KvParams p
 
 typedef void (*VecKernel)(const KvParams);
 
-template <class IT, int CPL>
+template <class IT, int CPL, bool PR>
 static VecKernel pick_ck(int ck, bool reg_gamma) {
     switch (ck) {
-        case OUT16: return reg_gamma ? kv_vec_kernel<IT, CPL, OUT16, true> : kv_vec_kernel<IT, CPL, OUT16, false>;
-        case OUT_I8: return kv_vec_kernel<IT, CPL, OUT_I8, false>;
-        case OUT_E4M3: return kv_vec_kernel<IT, CPL, OUT_E4M3, false>;
-        default: return kv_vec_kernel<IT, CPL, OUT_E5M2, false>;
+        case OUT16:
+            return reg_gamma ? kv_vec_kernel<IT, CPL, OUT16, true, PR> : kv_vec_kernel<IT, CPL, OUT16, false, PR>;
+        case OUT_I8: return kv_vec_kernel<IT, CPL, OUT_I8, false, PR>;
+        case OUT_E4M3: return kv_vec_kernel<IT, CPL, OUT_E4M3, false, PR>;
+        default: return kv_vec_kernel<IT, CPL, OUT_E5M2, false, PR>;
     }
 }
 
+template <class IT, bool PR>
+static VecKernel pick_cpl_pr(int cpl, int ck, bool reg_gamma) {
+    if (cpl == 1) return pick_ck<IT, 1, PR>(ck, reg_gamma);
+    if (cpl == 2) return pick_ck<IT, 2, PR>(ck, reg_gamma);
+    return pick_ck<IT, 4, PR>(ck, reg_gamma);
+}
+
 template <class IT>
-static VecKernel pick_cpl(int cpl, int ck, bool reg_gamma) {
-    if (cpl == 1) return pick_ck<IT, 1>(ck, reg_gamma);
-    if (cpl == 2) return pick_ck<IT, 2>(ck, reg_gamma);
-    return pick_ck<IT, 4>(ck, reg_gamma);
+static VecKernel pick_cpl(int cpl, int ck, bool reg_gamma, bool params_ready) {
+    return params_ready ? pick_cpl_pr<IT, true>(cpl, ck, reg_gamma) : pick_cpl_pr<IT, false>(cpl, ck, reg_gamma);
 }
 
 // Resident CTAs per SM for (kernel, dynamic shared memory), computed once and
@@ -294,8 +311,8 @@ cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, c
         // Register-held gamma for small batches into 16-bit caches (latency),
         // shared-memory constants otherwise (instructions per row).
         const bool reg_gamma = ckv_kind == OUT16 && p.T < KVR_REG_GAMMA_MAX_ROWS;
-        VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind, reg_gamma)
-                                            : pick_cpl<F16>(cpl, ckv_kind, reg_gamma);
+        VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind, reg_gamma, p.params_ready != 0)
+                                            : pick_cpl<F16>(cpl, ckv_kind, reg_gamma, p.params_ready != 0);
         const size_t smem = reg_gamma ? 0 : size_t(p.Dv) * 8 + size_t(p.Dk) * 4;
         const int threads = reg_gamma ? VecShape<true>::threads : VecShape<false>::threads;
         const int64_t ctas = (p.T + threads / 32 - 1) / (threads / 32);

@@ -170,6 +170,7 @@ kvr_status kv_plan(const kvr_kv_args* a, KvPlan* plan, bool* empty) {
     p.eps = a->eps;
     p.inv_dv = 1.0f / float(a->Dv);
     p.alpha = a->kc_scale;
+    p.params_ready = a->params_ready != 0;
 
     // Kernel path: the bulk-copy pipeline and the register path need 16-byte
     // rows (Dv, Dk multiples of 8, 16-byte aligned bases and row stride);

@@ -247,6 +247,7 @@ struct KvParams {
     int mode;            // kvr_cache_mode
     int k_kind;          // OutKind of the k cache
     int ckv_scale_per_ch, k_scale_per_ch;
+    int params_ready;    // gamma/scales may be read before the dependency wait
     float eps, inv_dv, alpha;
 };
 

@@ -518,7 +518,7 @@ def run_extras(dev, kvr, wl, flush_buf):
                 "frac_of_nominal_8000": gbs / 8000.0,
                 "gbs_isolated": nbytes / (us_iso / 1e6) / 1e9}
 
-    def kv_workload(make, seeds):
+    def kv_workload(make, seeds, params_ready=False):
         cases = [make(seed=s) for s in seeds]
         c0 = cases[0]
         ckv = torch.zeros(c0.cache_shapes()[0], dtype=wl.code_torch_dtype(c0.ckv_dtype), device=dev).view(
@@ -528,7 +528,8 @@ def run_extras(dev, kvr, wl, flush_buf):
         calls = []
         for c in cases:
             a = (c.kv.to(dev), c.gamma.to(dev), c.cos.to(dev), c.sin.to(dev), c.index.to(dev), ckv, kc)
-            kw = dict(cache_mode=c.mode, eps=c.eps, ckv_scale=None if c.ckv_scale is None else c.ckv_scale.to(dev))
+            kw = dict(cache_mode=c.mode, eps=c.eps, ckv_scale=None if c.ckv_scale is None else c.ckv_scale.to(dev),
+                      params_ready=params_ready)
             calls.append(lambda a=a, kw=kw: kvr.kv_rmsnorm_rope_cache(*a, **kw))
         for f in calls:
             f()
@@ -548,6 +549,9 @@ def run_extras(dev, kvr, wl, flush_buf):
 
     out["prefill_paged"] = kv_workload(wl.prefill_paged, [1003 + 7919 * i for i in range(3)])
     out["quant_fp8"] = kv_workload(wl.quant_fp8, [1004 + 7919 * i for i in range(nsets(4096 * 1416))])
+    # the same with params_ready: gamma and the scales read before the dependency wait
+    out["quant_fp8_params_ready"] = kv_workload(wl.quant_fp8, [1004 + 7919 * i for i in range(nsets(4096 * 1416))],
+                                                params_ready=True)
     out["tiny_norm"] = kv_workload(wl.tiny_norm, [1001])
 
     qs = [wl.qsa_prepare_workload(seed=1005 + 7919 * i) for i in range(nsets(17.3e6))]

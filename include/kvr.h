@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 3
+#define KVR_ABI_VERSION 4
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -130,6 +130,13 @@ typedef enum kvr_cache_mode {
  *   kc_scale   alpha_kv, multiplies the normalised part; pass 1.0f for none.
  *   dev_status optional int32 device word; KVR_DEVERR_INDEX is OR-ed in when
  *              an index entry is out of range (that token is skipped).
+ *   params_ready  0 (default): every input is read after the kernel waits for
+ *              the preceding kernel on the stream (programmatic dependent
+ *              launch). Nonzero: the caller promises that the kernel launched
+ *              immediately before this call on `stream` does not write gamma,
+ *              ckv_scale or k_scale (true of model weights and calibrated
+ *              scales); they may then be read before that wait, overlapping
+ *              the preceding kernel. Breaking the promise gives stale values.
  *
  * Limits: Dv >= 1, Dk >= 2 and even, Bkv, Skv >= 0, d0, d1 >= 1.
  * All arithmetic is float32 with one rounding to the cache type.
@@ -156,6 +163,7 @@ typedef struct kvr_kv_args {
     float eps;
     float kc_scale;
     int32_t* dev_status;
+    int32_t params_ready;
 } kvr_kv_args;
 
 kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);

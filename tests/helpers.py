@@ -111,7 +111,7 @@ def sentinel_cache(shape, dtype, dev="cuda"):
     return torch.full(shape, sentinel(dtype), dtype=code_torch_dtype(dtype), device=dev).view(TORCH_DTYPES[dtype])
 
 
-def run_gpu_kv(case, kv=None, ckv=None, k=None, dev="cuda"):
+def run_gpu_kv(case, kv=None, ckv=None, k=None, dev="cuda", params_ready=False):
     """Run the CUDA path on a KVCase; returns (ckv codes, k codes, status) as numpy/int."""
     import attention_prologue_kv_gb300 as kvr
     sh_ckv, sh_k = case.cache_shapes()
@@ -124,7 +124,7 @@ def run_gpu_kv(case, kv=None, ckv=None, k=None, dev="cuda"):
         case.sin.to(dev), case.index.to(dev), ckv, k, cache_mode=case.mode, eps=case.eps,
         ckv_scale=None if case.ckv_scale is None else case.ckv_scale.to(dev),
         k_scale=None if case.k_scale is None else case.k_scale.to(dev),
-        kc_scale=case.kc_scale, dev_status=status)
+        kc_scale=case.kc_scale, dev_status=status, params_ready=params_ready)
     torch.cuda.synchronize()
     return codes_of(ckv), codes_of(k), int(status.item())
 

@@ -189,6 +189,24 @@ def test_prepared_call_matches_the_plain_call_and_sees_new_contents():
     compare_cache(codes_of(k), r_k, "bf16", 64)
 
 
+@pytest.mark.parametrize("make", [
+    wl.decode_paged, wl.quant_fp8,
+    lambda: wl.make_kv_case("p", 8, 40, mode="PA_BSND", d0=8, d1=64, ckv_dtype="int8", k_dtype="fp8_e4m3fn",
+                            seed=64, skip=3, kv_std=3.0, scale_len=1),
+    lambda: wl.make_kv_case("p", 8, 40, mode="PA_BSND", d0=8, d1=64, ckv_dtype="fp8_e5m2", k_dtype="int8",
+                            seed=65, kv_std=3.0),
+    lambda: wl.make_kv_case("p", 4, 9, Dv=20, Dk=6, mode="PA_BSND", d0=4, d1=16, ckv_dtype="fp8_e4m3fn",
+                            k_dtype="int8", seed=66)],
+    ids=["decode_paged", "quant_fp8", "per_tensor_scales", "per_channel_k_scale", "generic_path"])
+def test_params_ready_gives_the_same_result(make):
+    """params_ready only moves the reads of gamma and the scales before the
+    dependency wait: the register flavour (decode), the shared-memory flavour
+    (quant), per-tensor and per-channel scales, and the generic path agree
+    with the oracle as without it."""
+    case = make()
+    check(case, params_ready=True)
+
+
 def test_staged_call_from_pinned_host_memory():
     """kv_rmsnorm_rope_cache_staged: two batches staged from pinned host
     memory into one device buffer, each followed by its call and a status
