@@ -41,14 +41,16 @@ __device__ __forceinline__ int dq_code(float x, float s) {
 // most 127 in magnitude, ulp(q0) <= 2^-17 there). Rounding q0 or fl32(x/s)
 // to an integer can therefore differ only when q0 lies within that distance
 // of a half-integer. With d = q0 - rint(q0) (|d| <= 1/2), the distance to the
-// nearest half-integer is 1/2 - |d|: `maxd` tracks the largest |d|, and when
-// it reaches 1/2 - 2^-15 the caller repairs those elements (dq_fix_near_ties).
+// nearest half-integer is 1/2 - |d|: bit `base + j` of `near` is set for
+// element j when |d| >= 1/2 - 2^-15, and the caller repairs those elements
+// (dq_fix_element).
 // Valid while 1/s is a normal float (the caller checks s >= 2^-100).
 // Rounding: with M = 1.5 * 2^23, t = fl(q0 + M) rounds q0 (|q0| < 2^22) to an
 // integer with ties to even inside the addition, and the low byte of t's bits
 // is that integer's two's-complement byte.
 template <class IT>
-__device__ __forceinline__ uint2 dq_chunk_fast(const uint4& x, float y, float& maxd) {
+__device__ __forceinline__ uint2 dq_chunk_fast(const uint4& x, float y, uint32_t& near, int base) {
+    const float T = 0.5f - 0x1p-15f;
     const float M = 12582912.0f;
     const float2 y2 = make_float2(y, y), M2 = make_float2(M, M), nM2 = make_float2(-M, -M),
                  m1 = make_float2(-1.f, -1.f);
@@ -60,7 +62,8 @@ __device__ __forceinline__ uint2 dq_chunk_fast(const uint4& x, float y, float& m
         const float2 t = __fadd2_rn(q0, M2);
         const float2 r = __fadd2_rn(t, nM2);          // rint(q0), exact
         const float2 d = __ffma2_rn(r, m1, q0);       // q0 - r, exact
-        maxd = fmaxf(maxd, fmaxf(fabsf(d.x), fabsf(d.y)));
+        near |= (fabsf(d.x) >= T ? 1u : 0u) << (base + 2 * k);
+        near |= (fabsf(d.y) >= T ? 1u : 0u) << (base + 2 * k + 1);
         b[k] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);   // two code bytes
     }
     return make_uint2(__byte_perm(b[0], b[1], 0x5410), __byte_perm(b[2], b[3], 0x5410));
@@ -79,25 +82,29 @@ __device__ __forceinline__ uint2 dq_chunk_exact(const uint4& x, float s) {
     return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
-// Repair the codes of dq_chunk_fast where the product lies within 2^-15 of a
-// half-integer: each such element (the same RN(x*y) and test as the fast
-// path) takes the IEEE division; the others keep their code. A warp runs
-// the division only at element positions where one of its lanes needs it
-// (on bfloat16 rows one element per warp on average, since q*127/m is often
-// a dyadic rational).
-template <class IT>
-__device__ __forceinline__ void dq_fix_near_ties(const uint4& x, float y, float s, uint2& o) {
-    const float T = 0.5f - 0x1p-15f;
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+// Repair one element's code (element e of this lane's chunks: chunk e / 8,
+// 16-bit lane e % 8) with the IEEE division. The element is picked from the
+// registers by selects, so the array never goes to local memory. On
+// bfloat16 rows such repairs are common (q*127/m is often a dyadic
+// rational): 0.2% of elements, but in 59% of warp-rows some lane has one,
+// usually a single element.
+template <class IT, int CPL>
+__device__ __forceinline__ void dq_fix_element(const uint4 (&x)[CPL], int e, float s, uint2 (&o)[CPL]) {
+    const int c = e >> 3, w = (e >> 1) & 3;
+    uint32_t word = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float v = (j & 1) ? IT::hi(w[j >> 1]) : IT::lo(w[j >> 1]);
-        const float q0 = __fmul_rn(v, y);
-        if (fabsf(__fsub_rn(q0, rintf(q0))) >= T) {
-            const uint32_t code = uint32_t(dq_code(v, s)) & 0xFFu;
-            const int sh = 8 * (j & 3);
-            if (j < 4) o.x = (o.x & ~(0xFFu << sh)) | (code << sh);
-            else o.y = (o.y & ~(0xFFu << sh)) | (code << sh);
+    for (int cc = 0; cc < CPL; ++cc) {
+        const uint32_t a = w == 0 ? x[cc].x : (w == 1 ? x[cc].y : (w == 2 ? x[cc].z : x[cc].w));
+        word = cc == c ? a : word;
+    }
+    const float v = (e & 1) ? IT::hi(word) : IT::lo(word);
+    const uint32_t code = uint32_t(dq_code(v, s)) & 0xFFu;
+    const int sh = 8 * (e & 3);
+#pragma unroll
+    for (int cc = 0; cc < CPL; ++cc) {
+        if (cc == c) {
+            if (e & 4) o[cc].y = (o[cc].y & ~(0xFFu << sh)) | (code << sh);
+            else o[cc].x = (o[cc].x & ~(0xFFu << sh)) | (code << sh);
         }
     }
 }
@@ -163,15 +170,15 @@ __global__ void __launch_bounds__(DQ_THREADS) dq_vec_kernel(const DqParams p) {
         const float y = fast ? __frcp_rn(s) : 0.f;
         char* dst = reinterpret_cast<char*>(p.out) + t * p.H;
         uint2 o[CPL];
-        float maxd = 0.f;
+        uint32_t near = 0;
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
-            if (c * 32 + lane < nch) o[c] = fast ? dq_chunk_fast<IT>(x[c], y, maxd) : dq_chunk_exact<IT>(x[c], s);
-        // A product within 2^-15 of a half-integer: repair those codes.
-        if (fast && !(maxd < 0.5f - 0x1p-15f)) {
-#pragma unroll
-            for (int c = 0; c < CPL; ++c)
-                if (c * 32 + lane < nch) dq_fix_near_ties<IT>(x[c], y, s, o[c]);
+            if (c * 32 + lane < nch) o[c] = fast ? dq_chunk_fast<IT>(x[c], y, near, 8 * c) : dq_chunk_exact<IT>(x[c], s);
+        // Products within 2^-15 of a half-integer: repair those codes.
+        while (near != 0) {
+            const int e = __ffs(near) - 1;
+            near &= near - 1;
+            dq_fix_element<IT, CPL>(x, e, s, o);
         }
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
