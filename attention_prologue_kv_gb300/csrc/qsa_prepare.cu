@@ -249,6 +249,9 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 #ifndef KVR_QSA_RAW_PREFETCH
 #define KVR_QSA_RAW_PREFETCH 1
 #endif
+#ifndef KVR_QSA_KL_PREFETCH
+#define KVR_QSA_KL_PREFETCH 1
+#endif
 #ifndef KVR_QSA_BULK_THREADS
 #define KVR_QSA_BULK_THREADS 128
 #endif
@@ -293,6 +296,12 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
             const int64_t nr = min(kbs, p.L - r0);
             prefetch_l2_bulk(static_cast<const uint16_t*>(p.raw) + (n * p.L + r0) * Di, uint32_t(nr * Di * 2));
         }
+#endif
+#if KVR_QSA_KL_PREFETCH
+        // The sequence's key_length entry, by its first CTA only (every CTA
+        // of the sequence reads it; one prefetch per sequence avoids a hot
+        // spot on its L2 line).
+        if (jl == 0) prefetch_l2(p.key_length + (p.key_length_per_seq ? n : 0));
 #endif
     }
     pdl_wait();
