@@ -601,6 +601,27 @@ def run_extras(dev, kvr, wl, flush_buf):
         out[name] = r
     del past_bk
 
+    # the same kernel at 8x the new tokens (32 x 16384): separates its fixed
+    # per-call latency from its streaming rate
+    qb = [wl.make_qsa_case("qsa_prepare_L16384", 32, 16384, Di=128, Dr=64, kbs=64, seed=1105 + 7919 * i,
+                           past_max=8192, Bcap=400) for i in range(3)]
+    bkb = torch.zeros(32, 400, 128, dtype=torch.bfloat16, device=dev)
+    calls = []
+    for q in qb:
+        a = (d(q.raw), bkb, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
+             d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
+        calls.append(lambda a=a: kvr.qsa_prepare(*a))
+    for f in calls:
+        f()
+    iso, _ = time_each(calls[0], 10, flush, stream)
+    steady = time_graph(calls, 8 * len(calls), stream)
+    nbl = qb[0].completed_blocks()
+    r = summary(iso * 1e3, steady * 1e3, qsa_algorithmic_bytes(nbl, 32, 64, 128, 64), 32 * 16384, "new_tokens")
+    r["blocks"] = nbl
+    r["sets"] = "%d input sets" % len(qb)
+    out["qsa_prepare_L16384"] = r
+    del qb, calls, bkb
+
     # DynamicQuant of q^N for one decode step (256 tokens x 128 heads x 512)
     qs = [wl.dynamic_quant_decode(seed=1006 + 7919 * i) for i in range(nsets(256 * 128 * 512 * 2))]
     rows, H = qs[0].numel() // qs[0].shape[-1], qs[0].shape[-1]
