@@ -7,17 +7,21 @@
 // "aclnnMlaPrologV3WeightNz" ("Formula", key path).
 //
 // Design (memory-bound stream, ~1 flop per byte, no tensor cores):
-//  * one warp per token row, grid-stride over rows, 4 warps per CTA, grid
-//    sized to the resident capacity of the GPU;
+//  * one warp per token row, grid-stride over rows, grid sized to the
+//    resident capacity of the GPU; 2-warp CTAs with gamma in registers for
+//    small batches into 16-bit caches (latency), 4-warp CTAs with gamma and
+//    the scales staged once per CTA in shared memory otherwise;
+//  * before the programmatic-dependent-launch wait each warp prefetches its
+//    first row into L2 (one 128-byte line per lane); with params_ready the
+//    constants are also read before the wait;
 //  * per row every lane issues its loads at once: the int64 index, 16-byte
 //    non-caching loads of the Dv part (CPL chunks of 8 elements per lane),
-//    and, on the first Dk/8 lanes, one 16-byte chunk of the Dk part (4 RoPE
-//    pairs) plus the four 8-byte cos/sin pieces those pairs need;
+//    and, on the first Dk/2 lanes, one RoPE pair plus its four cos/sin
+//    entries;
 //  * sum of squares in float32 with a warp butterfly, one rsqrt;
-//  * gamma (and per-channel scales) staged once per CTA in shared memory;
 //  * whole cache rows written with 16-byte (8-byte for 8-bit codes) stores:
-//    512 contiguous bytes per warp instruction for the Dv part, two 64-byte
-//    runs for the Dk part, so every 32-byte sector is fully written;
+//    512 contiguous bytes per warp instruction for the Dv part, so every
+//    32-byte sector is fully written;
 //  * index -1 skips the row; an out-of-range index skips it and raises
 //    KVR_DEVERR_INDEX. No atomics touch data.
 #include <map>

@@ -286,7 +286,8 @@ struct DqParams {
 
 // Launch with programmatic stream serialisation allowed: the grid may be
 // scheduled while the previous kernel on the stream drains; its kernels call
-// pdl_wait() before touching global memory.
+// pdl_wait() before reading global memory (before it they only issue L2
+// prefetches, and, when the caller sets params_ready, read gamma/scales).
 template <typename... Args>
 cudaError_t launch_pdl(void (*fn)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};

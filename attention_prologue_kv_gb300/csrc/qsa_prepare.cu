@@ -11,16 +11,22 @@
 // channels and rotate-half pairs on request). In the concat-output form the
 // past block keys are copied from past_block_index_keys first.
 //
-// Design: one CTA per (sequence, candidate block), 256 threads; the CTA
-// reads key_length on the device, derives the past length P = K - L, and
-// exits at once if its block is not completed by this call (no host sync).
-// Threads are laid out as (row group g, 16-byte channel chunk c): every
-// thread keeps kbs/G independent 16-byte loads in flight, sums them in
-// float32, and the G partial rows are reduced in shared memory. The mean,
-// the block-wide sum of squares, the rotation and one rounding to the
-// output type follow; the 2*Di-byte key row is written once. One extra CTA
-// per sequence writes the optional carry outputs, and in the concat-output
-// form `ncopy` more CTAs per sequence copy its past block-key rows.
+// Design: one CTA per (sequence, candidate block); the CTA reads key_length
+// on the device, derives the past length P = K - L, and exits at once if its
+// block is not completed by this call (no host sync). Two variants:
+//  * qsa_bulk_kernel (16-byte-aligned shapes up to 96 KB of rows): 128
+//    threads; before the dependency wait the CTA prefetches its slice of
+//    new keys into L2; after it, thread 0 reads key_length, derives the
+//    block's scalars once and pulls the block's rows, its first token's
+//    cos/sin and k_norm_weight into shared memory with bulk copies on one
+//    mbarrier; the CTA then sums the rows from shared memory;
+//  * qsa_kernel (any shape): 256 threads, each keeping kbs/G independent
+//    loads of a (row group g, channel chunk c) slice in flight.
+// Both reduce the G partial rows in shared memory, then take the mean, the
+// block-wide sum of squares, the rotation and one rounding to the output
+// type; the 2*Di-byte key row is written once. One extra CTA per sequence
+// writes the optional carry outputs, and in the concat-output form `ncopy`
+// more CTAs per sequence copy its past block-key rows.
 #include <mutex>
 #include <set>
 
@@ -252,6 +258,10 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 #ifndef KVR_QSA_KL_PREFETCH
 #define KVR_QSA_KL_PREFETCH 1
 #endif
+// Suspend-time hint (ns) of thread 0's polls of the copy barrier.
+#ifndef KVR_QSA_WAIT_SLEEP_NS
+#define KVR_QSA_WAIT_SLEEP_NS 128
+#endif
 #ifndef KVR_QSA_BULK_THREADS
 #define KVR_QSA_BULK_THREADS 128
 #endif
@@ -394,9 +404,6 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     // Thread 0 waits for the copies; the rest of the CTA sleeps in the barrier
     // (which also orders thread 0's observation before every thread's reads).
     __shared__ int timed_out;
-#ifndef KVR_QSA_WAIT_SLEEP_NS
-#define KVR_QSA_WAIT_SLEEP_NS 128
-#endif
     if (tid == 0) {
         timed_out = 0;
         if (!mbar_wait(bar, 0, nullptr, KVR_QSA_WAIT_SLEEP_NS)) {

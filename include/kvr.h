@@ -26,11 +26,13 @@
  *       path on "aclnnMlaPrologV3WeightNz": per-row int8 codes and scales.
  *
  * Conventions shared by every entry point
- *   - All tensor pointers are DEVICE pointers owned by the caller; the
- *     library allocates nothing and keeps no per-call state. Rows are dense
- *     and row-major unless a stride argument says otherwise.
+ *   - All tensor pointers are DEVICE pointers owned by the caller (the
+ *     host-staged entry point also takes pinned host buffers); the library
+ *     allocates nothing and keeps no per-call state. Rows are dense and
+ *     row-major unless a stride argument says otherwise.
  *   - Calls are asynchronous on `stream`: they validate on the host, launch,
- *     and return. Nothing is read back to the host.
+ *     and return. Nothing is read back to the host (except the status word
+ *     the host-staged entry point copies back, asynchronously).
  *   - Host-side errors (a NULL that is required, a bad shape, dtype or
  *     mode) are returned before any launch; nothing is written.
  *   - Data-dependent errors are found on the device: the offending row or
@@ -41,10 +43,14 @@
  *     its copies in flight land, and returns.
  *   - Each launch uses programmatic dependent launch: it may start while the
  *     previous kernel on the stream finishes, and waits for that kernel's
- *     results before it reads any input.
- *   - An empty problem (T = Bkv*Skv = 0, or N*L = 0) returns KVR_OK with no
+ *     results before it reads any input (the one exception is opt-in:
+ *     kvr_kv_args.params_ready lets gamma and the scales be read earlier).
+ *     Before the wait a kernel only issues L2 prefetches of its inputs.
+ *   - An empty problem (T = Bkv*Skv = 0, or N = 0) returns KVR_OK with no
  *     launch, mirroring the empty-tensor rule of "aclnnMlaPrologV3WeightNz"
- *     ("Shape restrictions": caches are not updated).
+ *     ("Shape restrictions": caches are not updated). A qsa_prepare call
+ *     with L = 0 launches only when it has carry outputs or a separate past
+ *     buffer to write.
  *   - Results are deterministic: no atomics touch data.
  *   - Thread safe: entry points may be called concurrently from any host
  *     thread on any stream; overlapping writes to the same cache rows from
