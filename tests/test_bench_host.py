@@ -56,3 +56,14 @@ def test_default_arguments_obey_the_contract():
     a = bench.parse_args([])
     assert a.gpus == 1 and a.warmup >= 3 and a.impl == "ours"
     assert bench.parse_args(["--warmup", "0"]).warmup == 3
+
+
+def test_kernel_source_hash_ignores_comments_not_code():
+    """The profiled-traffic guard keys on code: comments and layout do not
+    change it, any code or string-literal change does."""
+    import bench
+    a = 'x = 1; // note\n/* block\n comment */ asm("mov // not a comment");'
+    b = 'x = 1;\n\n   asm("mov // not a comment");   // other note'
+    assert bench._code_tokens(a) == bench._code_tokens(b)
+    assert bench._code_tokens(a) != bench._code_tokens(a.replace("x = 1", "x = 2"))
+    assert bench._code_tokens(a) != bench._code_tokens(a.replace("mov //", "mov2 //"))
