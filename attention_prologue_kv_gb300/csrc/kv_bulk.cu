@@ -38,9 +38,18 @@ namespace kvr {
 #endif
 constexpr int BULK_CONSUMERS = KVR_BULK_CONSUMERS;
 constexpr int BULK_THREADS = 32 * (1 + BULK_CONSUMERS);
+// Resident CTAs per SM (each with its own ring of KVR_BULK_RING_KB).
+#ifndef KVR_BULK_CTAS_PER_SM
+#define KVR_BULK_CTAS_PER_SM 1
+#endif
+// Before the dependency wait, prefetch this CTA's first KVR_BULK_PREFETCH
+// ring-fulls of tiles into L2 (a hint only: L2 is the coherence point).
+#ifndef KVR_BULK_PREFETCH
+#define KVR_BULK_PREFETCH 1
+#endif
 
 template <class IT, int CPL, int CK>
-__global__ void __launch_bounds__(BULK_THREADS, 1) kv_bulk_kernel(const KvParams p) {
+__global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_kernel(const KvParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + p.S;
@@ -66,6 +75,18 @@ __global__ void __launch_bounds__(BULK_THREADS, 1) kv_bulk_kernel(const KvParams
         }
         *abort_flag = 0;
         fence_mbar_init();
+#if KVR_BULK_PREFETCH
+        int64_t it = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && it < int64_t(KVR_BULK_PREFETCH) * p.S;
+             tile += gridDim.x, ++it) {
+            const int64_t r0 = tile * p.R;
+            const int rows = int(p.T - r0 < p.R ? p.T - r0 : p.R);
+            if (p.kv_contig) prefetch_l2_bulk(static_cast<const char*>(p.kv) + r0 * kv_row, rows * kv_row);
+            prefetch_l2_bulk(static_cast<const char*>(p.cos) + r0 * cs_row, rows * cs_row);
+            prefetch_l2_bulk(static_cast<const char*>(p.sin) + r0 * cs_row, rows * cs_row);
+            if (p.idx_bulk && rows >= 2) prefetch_l2_bulk(p.index + r0, uint32_t(rows & ~1) * 8);
+        }
+#endif
     }
     __syncthreads();
     pdl_wait();
@@ -229,10 +250,8 @@ static cudaError_t ensure_smem(BulkKernel fn) {
 cudaError_t launch_kv_bulk(const KvParams& p0, int in_dtype, int ckv_kind, cudaStream_t s) {
     KvParams p = p0;
     const int sms = sm_count_current_device();
-    // Rows per tile: 8 when every SM gets several tiles, fewer for small
-    // batches so that the tiles still spread over the SMs.
-    // Rows per tile: up to 16, fewer when that still leaves each CTA at least
-    // four tiles (load balance across the SMs).
+    // Rows per tile: up to KVR_BULK_MAX_ROWS, halved while that leaves fewer
+    // than four tiles per SM (load balance across the SMs).
     int R = KVR_BULK_MAX_ROWS;
     while (R > 2 && (p.T + R - 1) / R < int64_t(4) * sms) R >>= 1;
     const uint32_t kv_row = uint32_t(p.Dv + p.Dk) * 2;
@@ -257,7 +276,8 @@ cudaError_t launch_kv_bulk(const KvParams& p0, int in_dtype, int ckv_kind, cudaS
     cudaError_t e = ensure_smem(fn);
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (p.T + R - 1) / R;
-    const int grid = int(ntiles < sms ? ntiles : sms);
+    const int64_t slots = int64_t(sms) * KVR_BULK_CTAS_PER_SM;
+    const int grid = int(ntiles < slots ? ntiles : slots);
     return launch_pdl(fn, dim3(grid), dim3(BULK_THREADS), smem, s, p);
 }
 
