@@ -103,6 +103,13 @@ def _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ck
             raise ValueError("%s must have kv's dtype" % name)
     if index.dtype != torch.int64:
         raise ValueError("index must be int64")
+    # The kernels read exactly this many index entries (one per token, or one
+    # per BlockSize tokens of a sequence in PA_BLK_BSND); the C ABI cannot
+    # check a buffer's length, so the binding does.
+    n_index = Bkv * (-(-Skv // d1) if cache_mode == "PA_BLK_BSND" else Skv)
+    if index.numel() != n_index:
+        raise ValueError("index must have %d entries for %s (Bkv=%d, Skv=%d), got %d"
+                         % (n_index, cache_mode, Bkv, Skv, index.numel()))
     for t, name in ((ckv_scale, "ckv_scale"), (k_scale, "k_scale")):
         if t is not None and t.dtype != torch.float32:
             raise ValueError("%s must be float32" % name)

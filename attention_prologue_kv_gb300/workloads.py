@@ -99,8 +99,8 @@ def make_kv_case(name, Bkv, Skv, Dv=512, Dk=64, mode="PA_BSND", d0=None, d1=128,
     pos       "random": one random position per token in [0, pos_max);
               "start": a random start in [0, pos_max) per sequence, + s;
               "seq": position s
-    row_pad   extra elements after each kv row (kv becomes a column slice of a
-              wider [T, D + row_pad] buffer: a strided row)
+    row_pad   extra elements after each kv row (kv becomes a [Bkv, 1, Skv, D]
+              view of a wider [T, D + row_pad] buffer: strided rows)
     """
     g = torch.Generator().manual_seed(seed)
     dt = TORCH_DTYPES[in_dtype]
@@ -108,7 +108,7 @@ def make_kv_case(name, Bkv, Skv, Dv=512, Dk=64, mode="PA_BSND", d0=None, d1=128,
     T = Bkv * Skv
     wide = torch.randn(T, D + row_pad, generator=g, dtype=torch.float32) * kv_std
     wide = wide.to(dt)
-    kv = wide[:, :D].view(Bkv, 1, Skv, D) if row_pad == 0 else wide[:, :D]
+    kv = wide[:, :D].view(Bkv, 1, Skv, D)   # strided rows when row_pad > 0
     gamma = (torch.rand(Dv, generator=g, dtype=torch.float32) + 0.5).to(dt)
 
     if pos == "random":

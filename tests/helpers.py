@@ -90,6 +90,7 @@ def run_oracle_qsa(case, block_keys=None, carry=False, rope_layout="interleave_l
         npr = np.full((case.N, 2 * case.Dr), np.nan) if case.Dr else None
     st = oracle.ref_qsa_prepare(block_keys=block_keys, next_raw=nr, next_rope=npr,
                                 rope_layout=rope_layout, past_block_keys=past_block_keys,
+                                out_dtype="f16" if case.raw.dtype == torch.float16 else "bf16",
                                 **oracle_qsa_inputs(case))
     return block_keys, nr, npr, st
 
@@ -102,7 +103,7 @@ def kv_to_device(case, dev="cuda"):
     """The case's kv on the device, keeping a strided-row layout when the case has one."""
     D = case.Dv + case.Dk
     if case.meta.get("row_pad"):
-        return case.meta["wide"].to(dev)[:, :D]
+        return case.meta["wide"].to(dev)[:, :D].view(case.Bkv, 1, case.Skv, D)
     return case.kv.to(dev)
 
 

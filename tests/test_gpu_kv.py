@@ -96,6 +96,22 @@ def test_strided_rows(pad):
     check(case)
 
 
+def test_index_length_is_checked_against_the_cache_mode():
+    """The kernels read one index entry per token (one per BlockSize tokens in
+    PA_BLK_BSND); a shorter index is refused before launch."""
+    import attention_prologue_kv_gb300 as kvr
+    case = wl.make_kv_case("x", 3, 20, mode="PA_BLK_BSND", d0=12, d1=8, seed=67)
+    assert case.index.numel() == 3 * 3
+    ckv = sentinel_cache(case.cache_shapes()[0], "bf16")
+    k = sentinel_cache(case.cache_shapes()[1], "bf16")
+    args = (case.kv.cuda(), case.gamma.cuda(), case.cos.cuda(), case.sin.cuda())
+    with pytest.raises(ValueError):
+        kvr.kv_rmsnorm_rope_cache(*args, case.index[:8].cuda(), ckv, k, cache_mode="PA_BLK_BSND")
+    with pytest.raises(ValueError):   # the flattened (T, D) form implies one entry per token
+        kvr.kv_rmsnorm_rope_cache(args[0].view(60, -1), args[1], args[2].view(60, -1), args[3].view(60, -1),
+                                  case.index.cuda(), ckv, k, cache_mode="PA_BLK_BSND")
+
+
 def test_misaligned_pointers_take_the_generic_path():
     case = wl.make_kv_case("u", 5, 11, mode="PA_BSND", d0=2, d1=64, seed=48)
     T, D = case.T, case.Dv + case.Dk
