@@ -113,6 +113,11 @@ def _kv_args(kv, gamma, cos, sin, index, ckv_cache, k_cache, cache_mode, eps, ck
     for t, name in ((ckv_scale, "ckv_scale"), (k_scale, "k_scale")):
         if t is not None and t.dtype != torch.float32:
             raise ValueError("%s must be float32" % name)
+    for t, name in ((cos, "cos"), (sin, "sin")):
+        if t.numel() != Bkv * Skv * Dk:
+            raise ValueError("%s must have Bkv*Skv*Dk = %d elements, got %d" % (name, Bkv * Skv * Dk, t.numel()))
+    if dev_status is not None and dev_status.numel() < 1:
+        raise ValueError("dev_status must have one element")
     if dev_status is not None and dev_status.dtype != torch.int32:
         raise ValueError("dev_status must be int32")
     return N.KvArgs(
@@ -253,6 +258,22 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
     if dev_status is not None and dev_status.dtype != torch.int32:
         raise ValueError("dev_status must be int32")
     Dr = rope_cos.shape[-1] if rope_cos is not None else 0
+    # The C ABI cannot check a buffer's length: every tensor the kernels read
+    # or write must have exactly the size its role implies.
+    kbs = int(key_block_size)
+    sizes = ((rope_cos, "rope_cos", Nn * L * Dr), (rope_sin, "rope_sin", Nn * L * Dr),
+             (k_norm_weight, "k_norm_weight", Di),
+             (past_incomplete_raw_keys, "past_incomplete_raw_keys", Nn * (kbs - 1) * Di),
+             (past_incomplete_rope, "past_incomplete_rope", Nn * 2 * Dr),
+             (next_incomplete_raw_keys, "next_incomplete_raw_keys", Nn * (kbs - 1) * Di),
+             (next_incomplete_rope, "next_incomplete_rope", Nn * 2 * Dr))
+    for t, name, n in sizes:
+        if t is not None and kbs > 1 and t.numel() != n:
+            raise ValueError("%s must have %d elements, got %d" % (name, n, t.numel()))
+    if key_length.numel() not in (1, Nn):
+        raise ValueError("key_length must have 1 or N elements")
+    if dev_status is not None and dev_status.numel() < 1:
+        raise ValueError("dev_status must have one element")
     a = N.QsaArgs(
         raw_index_keys=_ptr(raw, "raw_index_keys"), in_dtype=_IN_DTYPES[raw.dtype], N=Nn, L=L, Di=Di,
         block_keys=_ptr(block_keys, "block_keys"), Bcap=block_keys.shape[1],

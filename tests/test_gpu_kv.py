@@ -107,6 +107,9 @@ def test_index_length_is_checked_against_the_cache_mode():
     args = (case.kv.cuda(), case.gamma.cuda(), case.cos.cuda(), case.sin.cuda())
     with pytest.raises(ValueError):
         kvr.kv_rmsnorm_rope_cache(*args, case.index[:8].cuda(), ckv, k, cache_mode="PA_BLK_BSND")
+    with pytest.raises(ValueError):   # cos shorter than one entry row per token
+        kvr.kv_rmsnorm_rope_cache(args[0], args[1], args[2][:2].contiguous(), args[3], case.index.cuda(), ckv, k,
+                                  cache_mode="PA_BLK_BSND")
     with pytest.raises(ValueError):   # the flattened (T, D) form implies one entry per token
         kvr.kv_rmsnorm_rope_cache(args[0].view(60, -1), args[1], args[2].view(60, -1), args[3].view(60, -1),
                                   case.index.cuda(), ckv, k, cache_mode="PA_BLK_BSND")

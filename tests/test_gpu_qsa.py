@@ -205,3 +205,24 @@ def test_chained_concat_calls_equal_one_call():
         prev, past_raw, past_rope = out, nr, npr
     torch.cuda.synchronize()
     assert np.array_equal(prev.cpu().view(torch.int16).numpy(), whole.view(np.int16))
+
+
+def test_buffer_lengths_are_checked():
+    """Tables, weights and carry buffers of the wrong length are refused
+    before launch (the C ABI cannot see a buffer's length)."""
+    import attention_prologue_kv_gb300 as kvr
+    case = wl.make_qsa_case("b", 3, 20, Di=32, Dr=8, kbs=4, seed=40)
+    d = lambda t: t.cuda()
+    bk = torch.zeros(3, case.Bcap, 32, dtype=torch.bfloat16, device="cuda")
+    args = [d(case.raw), bk, d(case.key_length), d(case.rope_cos), d(case.rope_sin), d(case.k_norm_weight),
+            d(case.past_raw), d(case.past_rope), case.kbs]
+    for pos, short in ((3, d(case.rope_cos[:, :10]).contiguous()), (5, d(case.k_norm_weight[:16])),
+                       (6, d(case.past_raw[:2])), (7, d(case.past_rope[:, :8]).contiguous())):
+        bad = list(args)
+        bad[pos] = short
+        with pytest.raises(ValueError):
+            kvr.qsa_prepare(*bad)
+    with pytest.raises(ValueError):
+        kvr.qsa_prepare(*args, next_incomplete_raw_keys=torch.zeros(3, 2, 32, dtype=torch.bfloat16, device="cuda"))
+    kvr.qsa_prepare(*args)   # the well-formed call still runs
+    torch.cuda.synchronize()
