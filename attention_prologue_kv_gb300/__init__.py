@@ -6,5 +6,5 @@ libkvr.so (include/kvr.h); this package holds the thin ctypes binding, the
 build step and the seeded synthetic workloads. There is no CPU fallback:
 calling an entry point without the built library raises.
 """
-from .api import (KvrError, PreparedCall, device_copy, dynamic_quant,  # noqa: E402,F401
-                  kv_rmsnorm_rope_cache, prepare_kv_rmsnorm_rope_cache, qsa_prepare)
+from .api import (KvrError, PreparedCall, check_bounded_wait, device_copy,  # noqa: E402,F401
+                  dynamic_quant, kv_rmsnorm_rope_cache, prepare_kv_rmsnorm_rope_cache, qsa_prepare)

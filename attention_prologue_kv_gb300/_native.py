@@ -5,7 +5,7 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvr.so")
-ABI_VERSION = 4   # KVR_ABI_VERSION of include/kvr.h these structures mirror
+ABI_VERSION = 5   # KVR_ABI_VERSION of include/kvr.h these structures mirror
 
 # kvr_status
 KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS, KVR_ERR_CUDA = range(7)
@@ -67,6 +67,7 @@ class DqArgs(ctypes.Structure):
 
 
 EXPORTS = ("kv_rmsnorm_rope_cache", "kv_rmsnorm_rope_cache_staged", "qsa_prepare", "dynamic_quant", "kvr_device_copy",
+           "kvr_check_bounded_wait",
            "kvr_status_string", "kvr_abi_version")
 
 _lib = None
@@ -92,6 +93,8 @@ def lib():
     L.qsa_prepare.restype = _int
     L.dynamic_quant.argtypes = [ctypes.POINTER(DqArgs), _vp]
     L.dynamic_quant.restype = _int
+    L.kvr_check_bounded_wait.argtypes = [_vp, _i64, _i64, _vp]
+    L.kvr_check_bounded_wait.restype = _int
     L.kvr_device_copy.argtypes = [_vp, _vp, _i64, _vp]
     L.kvr_device_copy.restype = _int
     L.kvr_status_string.argtypes = [_int]

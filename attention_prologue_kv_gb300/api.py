@@ -294,6 +294,19 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
         raise KvrError(st, "qsa_prepare")
 
 
+def check_bounded_wait(dev_status, limit_us, abort_after_us=0, stream=None):
+    """Failure-detection check: a kernel waits for an mbarrier phase that
+    never completes and gives up after `limit_us` microseconds (or when a
+    second warp raises the abort flag after `abort_after_us`), OR-ing
+    KVR_DEVERR_TIMEOUT into `dev_status` (int32, device). Asynchronous."""
+    if dev_status.dtype != torch.int32 or dev_status.numel() < 1:
+        raise ValueError("dev_status must be an int32 tensor with one element")
+    st = N.lib().kvr_check_bounded_wait(_ptr(dev_status, "dev_status"), int(limit_us * 1000),
+                                        int(abort_after_us * 1000), _stream(stream))
+    if st != N.KVR_OK:
+        raise KvrError(st, "kvr_check_bounded_wait")
+
+
 def dynamic_quant(q_nope, q_out, dequant_scale, *, stream=None):
     """DynamicQuant of q^N: per row (last axis, e.g. q^N [T, N, Hckv] gives
     T*N rows) dequant_scale = RowMax(|q|)/127 and q_out = round(q/scale) as

@@ -1,0 +1,50 @@
+// Exercise of the bounded-wait path the pipeline kernels rely on: a warp
+// waits on an mbarrier phase that can never complete (it expects bytes that
+// no copy delivers), polling the way mbar_wait does, and gives up when the
+// time limit passes or when another warp raises the abort flag. The kernel
+// then records KVR_DEVERR_TIMEOUT and returns, leaving the context usable.
+// No copy is in flight, so the CTA may exit with the phase pending.
+#include "kvr_internal.cuh"
+
+namespace kvr {
+
+__global__ void __launch_bounds__(64) bounded_wait_kernel(int32_t* status, uint64_t limit_ns, uint64_t abort_after_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        int ok = 1;
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(&bar, 16);   // 16 bytes that will never arrive
+            ok = 0;
+            const uint64_t t0 = globaltimer_ns();
+            for (;;) {
+                __nanosleep(64);
+                if (mbar_try_wait(&bar, 0)) {
+                    ok = 1;
+                    break;
+                }
+                if (abort_flag) break;
+                if (globaltimer_ns() - t0 > limit_ns) break;
+            }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok && threadIdx.x == 0) atomicOr(status, KVR_DEVERR_TIMEOUT);
+    } else if (threadIdx.x == 32 && abort_after_ns > 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < abort_after_ns) __nanosleep(256);
+        abort_flag = 1;
+    }
+}
+
+cudaError_t launch_bounded_wait(int32_t* status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t s) {
+    bounded_wait_kernel<<<1, 64, 0, s>>>(status, uint64_t(limit_ns), uint64_t(abort_after_ns));
+    return cudaGetLastError();
+}
+
+}  // namespace kvr

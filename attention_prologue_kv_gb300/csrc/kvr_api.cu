@@ -46,6 +46,9 @@ cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaSt
     return cudaGetLastError();
 }
 
+// Defined in bounded_wait.cu.
+cudaError_t launch_bounded_wait(int32_t* status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t s);
+
 }  // namespace kvr
 
 using namespace kvr;
@@ -338,6 +341,15 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
                       aligned(a->past_incomplete_rope, 16) && aligned(a->k_norm_weight, 16);
     (void)cudaGetLastError();
     return cuda_status(launch_qsa(p, a->in_dtype, vec, bulk, stream));
+}
+
+kvr_status kvr_check_bounded_wait(int32_t* dev_status, int64_t limit_ns, int64_t abort_after_ns,
+                                  cudaStream_t stream) {
+    if (dev_status == nullptr) return KVR_ERR_NULL;
+    if (limit_ns < 1000 || limit_ns > 1000000000 || abort_after_ns < 0 || abort_after_ns > limit_ns)
+        return KVR_ERR_SHAPE;
+    (void)cudaGetLastError();
+    return cuda_status(launch_bounded_wait(dev_status, limit_ns, abort_after_ns, stream));
 }
 
 kvr_status dynamic_quant(const kvr_dq_args* a, cudaStream_t stream) {

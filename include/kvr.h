@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 4
+#define KVR_ABI_VERSION 5
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -312,6 +312,16 @@ kvr_status dynamic_quant(const kvr_dq_args* args, cudaStream_t stream);
  * 16-byte aligned), used to measure the achievable HBM bandwidth in the same
  * process as the kernels above. */
 kvr_status kvr_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
+
+/* Failure-detection check (no counterpart on the pages): one small kernel
+ * waits, the way the pipeline kernels wait on their copies, for an mbarrier
+ * phase that never completes (it expects bytes that no copy delivers). It
+ * gives up after `limit_ns` nanoseconds (1e3 .. 1e9), or after
+ * `abort_after_ns` (0 = never; at most limit_ns) when a second warp raises
+ * the abort flag the pipelines use, then ORs KVR_DEVERR_TIMEOUT into the
+ * device word *dev_status and returns: nothing traps and the context stays
+ * usable. Asynchronous on `stream`. */
+kvr_status kvr_check_bounded_wait(int32_t* dev_status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char* kvr_status_string(kvr_status status);

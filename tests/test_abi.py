@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.kvr_abi_version() == N.ABI_VERSION == 4
+    assert lib.kvr_abi_version() == N.ABI_VERSION == 5
 
 
 def test_status_strings(lib):
@@ -230,3 +230,10 @@ def test_python_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         kvr.kv_rmsnorm_rope_cache(x, x[0, 0, 0, :512], x, x, torch.zeros(6, dtype=torch.int64),
                                   x, x)
+
+
+def test_bounded_wait_check_validation(lib):
+    assert lib.kvr_check_bounded_wait(None, 100000, 0, None) == N.KVR_ERR_NULL
+    assert lib.kvr_check_bounded_wait(1 << 20, 10, 0, None) == N.KVR_ERR_SHAPE            # limit below 1 us
+    assert lib.kvr_check_bounded_wait(1 << 20, 2 * 10**9, 0, None) == N.KVR_ERR_SHAPE      # above 1 s
+    assert lib.kvr_check_bounded_wait(1 << 20, 100000, 200000, None) == N.KVR_ERR_SHAPE    # abort after the limit
