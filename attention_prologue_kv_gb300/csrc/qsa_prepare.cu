@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 #ifndef KVR_QSA_RAW_PREFETCH
 #define KVR_QSA_RAW_PREFETCH 1
 #endif
+#ifndef KVR_QSA_SPECIALISE
+#define KVR_QSA_SPECIALISE 1
+#endif
 #ifndef KVR_QSA_KL_PREFETCH
 #define KVR_QSA_KL_PREFETCH 1
 #endif
@@ -267,12 +270,15 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 #endif
 constexpr int QSA_BULK_THREADS = KVR_QSA_BULK_THREADS;
 
-template <class IT>
+// DI / KBS: the key width and block size when fixed at compile time (0: read
+// from the parameters); a fixed shape turns the divisions, modulos and loop
+// bounds that depend on them into constants.
+template <class IT, int DI, int KBS>
 __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    const int Di = p.Di;
-    const int64_t kbs = p.kbs;
+    const int Di = DI ? DI : p.Di;
+    const int64_t kbs = KBS ? KBS : p.kbs;
     unsigned char* rows_s = smem + 128;                                      // kbs x Di 16-bit
     uint16_t* w_s = reinterpret_cast<uint16_t*>(rows_s + kbs * Di * 2);      // k_norm_weight [Di]
     uint16_t* rope_s = w_s + Di;                                             // [cos | sin] of the first token
@@ -482,6 +488,32 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     }
 }
 
+typedef void (*QsaKernel)(const QsaParams);
+
+// Compile-time shapes for common key widths and block sizes (per-block
+// instruction count is what bounds a small call: 4.85 vs 5.92 us on the
+// 32 x 2048-token workload); any other shape takes the runtime-shape kernel.
+template <class IT, int DI>
+static QsaKernel pick_qsa_kbs(int64_t kbs) {
+    switch (kbs) {
+        case 32: return qsa_bulk_kernel<IT, DI, 32>;
+        case 64: return qsa_bulk_kernel<IT, DI, 64>;
+        case 128: return qsa_bulk_kernel<IT, DI, 128>;
+        default: return nullptr;
+    }
+}
+
+template <class IT>
+static QsaKernel pick_qsa_bulk(int Di, int64_t kbs) {
+    QsaKernel fn = nullptr;
+#if KVR_QSA_SPECIALISE
+    if (Di == 64) fn = pick_qsa_kbs<IT, 64>(kbs);
+    else if (Di == 128) fn = pick_qsa_kbs<IT, 128>(kbs);
+    else if (Di == 256) fn = pick_qsa_kbs<IT, 256>(kbs);
+#endif
+    return fn != nullptr ? fn : qsa_bulk_kernel<IT, 0, 0>;
+}
+
 // Shared memory the bulk variant needs (0 if it does not fit).
 static size_t qsa_bulk_smem(const QsaParams& p) {
     const int C = p.Di / 8;
@@ -495,7 +527,7 @@ cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, cu
     const int64_t grid = p.N * (p.nbmax + 1 + p.ncopy);
     const size_t bsmem = bulk ? qsa_bulk_smem(p) : 0;
     if (bsmem > 0) {
-        auto fn = in_dtype == KVR_BF16 ? qsa_bulk_kernel<BF16> : qsa_bulk_kernel<F16>;
+        QsaKernel fn = in_dtype == KVR_BF16 ? pick_qsa_bulk<BF16>(p.Di, p.kbs) : pick_qsa_bulk<F16>(p.Di, p.kbs);
         if (bsmem > 48 * 1024) {
             static std::mutex mu;
             static std::set<const void*> done;

@@ -226,3 +226,26 @@ def test_buffer_lengths_are_checked():
         kvr.qsa_prepare(*args, next_incomplete_raw_keys=torch.zeros(3, 2, 32, dtype=torch.bfloat16, device="cuda"))
     kvr.qsa_prepare(*args)   # the well-formed call still runs
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("Di", [64, 128, 256])
+@pytest.mark.parametrize("kbs", [32, 64, 128])
+def test_compile_time_shapes(Di, kbs):
+    """The kernels compiled for fixed (Di, kbs) pairs, with the carry outputs
+    and a RoPE layout that changes from case to case."""
+    layout = ["interleave_last", "half_first", "interleave_first", "half_last"][(Di // 64 + kbs // 32) % 4]
+    case = wl.make_qsa_case("sp", 4, 300, Di=Di, Dr=min(64, Di), kbs=kbs, seed=Di + kbs, past_max=600)
+    n, _ = check(case, rope_layout=layout)
+    assert n == case.completed_blocks()
+
+
+@pytest.mark.parametrize("rope,norm", [(False, True), (True, False)])
+def test_compile_time_shape_features_disabled(rope, norm):
+    case = wl.make_qsa_case("sp", 5, 200, Di=128, Dr=64, kbs=64, seed=77, rope=rope, norm=norm, past_max=500)
+    check(case)
+
+
+def test_compile_time_shape_concat_form():
+    case = wl.make_qsa_case("sp", 6, 256, Di=128, Dr=64, kbs=32, seed=78, past_max=700)
+    P = np.array(case.meta["past"])
+    check(case, past_block_keys=_past_codes(case, int((P // 32).max()) + 2, 79))
