@@ -20,6 +20,9 @@
 namespace kvr {
 
 constexpr int DQ_THREADS = 128;
+#ifndef KVR_DQ_SPECIALISE
+#define KVR_DQ_SPECIALISE 1
+#endif
 constexpr int DQ_WARPS = DQ_THREADS / 32;
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -132,14 +135,15 @@ __device__ __forceinline__ uint32_t absmax2<F16>(uint32_t acc, uint32_t w) {
 // 8-byte aligned. Rows are double-buffered in registers: the loads of a
 // warp's next row are issued before the current row is quantised, so every
 // warp keeps two rows (2 KB for H = 512) in flight.
-template <class IT, int CPL>
+template <class IT, int CPL, int HC>
 __global__ void __launch_bounds__(DQ_THREADS) dq_vec_kernel(const DqParams p) {
     const int lane = threadIdx.x & 31;
-    const int nch = int(p.H >> 3);
+    const int64_t H = HC ? HC : p.H;   // row length, a constant when compiled for one
+    const int nch = int(H >> 3);
     const int64_t stride_rows = int64_t(gridDim.x) * DQ_WARPS;
     int64_t t = int64_t(blockIdx.x) * DQ_WARPS + (threadIdx.x >> 5);
     if (t < p.rows && lane == 0)
-        prefetch_l2_bulk(static_cast<const char*>(p.q) + t * p.q_stride * 2, uint32_t(p.H) * 2);
+        prefetch_l2_bulk(static_cast<const char*>(p.q) + t * p.q_stride * 2, uint32_t(H) * 2);
     pdl_wait();
     pdl_launch_dependents();
     uint4 x[CPL], nx[CPL];
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(DQ_THREADS) dq_vec_kernel(const DqParams p) {
         const float s = __fdiv_rn(m, 127.f);
         const bool fast = s >= 0x1p-100f;
         const float y = fast ? __frcp_rn(s) : 0.f;
-        char* dst = reinterpret_cast<char*>(p.out) + t * p.H;
+        char* dst = reinterpret_cast<char*>(p.out) + t * H;
         uint2 o[CPL];
         uint32_t near = 0;
 #pragma unroll
@@ -233,11 +237,17 @@ cudaError_t launch_dq(const DqParams& p, int in_dtype, bool vec, cudaStream_t s)
     if (vec) {
         const int nch = int(p.H / 8);
         const int cpl = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
+        const bool bf = in_dtype == KVR_BF16;
         K fn;
-        if (in_dtype == KVR_BF16)
-            fn = cpl == 1 ? dq_vec_kernel<BF16, 1> : (cpl == 2 ? dq_vec_kernel<BF16, 2> : dq_vec_kernel<BF16, 4>);
+        // Compiled row lengths (512 is the MLA query's Hckv): the per-chunk
+        // bounds tests and row offsets become constants.
+        if (KVR_DQ_SPECIALISE && p.H == 512) fn = bf ? dq_vec_kernel<BF16, 2, 512> : dq_vec_kernel<F16, 2, 512>;
+        else if (KVR_DQ_SPECIALISE && p.H == 256) fn = bf ? dq_vec_kernel<BF16, 1, 256> : dq_vec_kernel<F16, 1, 256>;
+        else if (KVR_DQ_SPECIALISE && p.H == 1024) fn = bf ? dq_vec_kernel<BF16, 4, 1024> : dq_vec_kernel<F16, 4, 1024>;
+        else if (bf)
+            fn = cpl == 1 ? dq_vec_kernel<BF16, 1, 0> : (cpl == 2 ? dq_vec_kernel<BF16, 2, 0> : dq_vec_kernel<BF16, 4, 0>);
         else
-            fn = cpl == 1 ? dq_vec_kernel<F16, 1> : (cpl == 2 ? dq_vec_kernel<F16, 2> : dq_vec_kernel<F16, 4>);
+            fn = cpl == 1 ? dq_vec_kernel<F16, 1, 0> : (cpl == 2 ? dq_vec_kernel<F16, 2, 0> : dq_vec_kernel<F16, 4, 0>);
         const int64_t cap = int64_t(dq_ctas_per_sm(reinterpret_cast<const void*>(fn))) * sms;
         return launch_pdl(fn, dim3(int(ctas < cap ? ctas : cap)), dim3(DQ_THREADS), size_t(0), s, p);
     }

@@ -47,7 +47,8 @@ struct RowRegs {
 };
 
 template <int CPL>
-__device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane, int nch, int h, RowRegs& r) {
+__device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane, int nch, int h, int Dv, int Dk,
+                                         RowRegs& r) {
     r.v = ld_stream_s64(p.index + index_pos(p, t));
     const char* x = static_cast<const char*>(p.kv) + t * p.kv_stride * 2;
 #pragma unroll
@@ -56,9 +57,9 @@ __device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane,
         if (ch < nch) r.x[c] = ld_stream_v4(x + ch * 16);
     }
     if (lane < h) {
-        r.xp = ld_stream_u32(x + int64_t(p.Dv) * 2 + lane * 4);
-        const uint16_t* cr = static_cast<const uint16_t*>(p.cos) + t * p.Dk;
-        const uint16_t* sr = static_cast<const uint16_t*>(p.sin) + t * p.Dk;
+        r.xp = ld_stream_u32(x + int64_t(Dv) * 2 + lane * 4);
+        const uint16_t* cr = static_cast<const uint16_t*>(p.cos) + t * Dk;
+        const uint16_t* sr = static_cast<const uint16_t*>(p.sin) + t * Dk;
         r.c0 = ld_stream_u16(cr + lane);
         r.c1 = ld_stream_u16(cr + h + lane);
         r.s0 = ld_stream_u16(sr + lane);
@@ -75,6 +76,9 @@ __device__ __forceinline__ void load_row(const KvParams& p, int64_t t, int lane,
 //    starts as soon as its loads land (lowest latency);
 //  * otherwise gamma and the scales are staged once per CTA in shared
 //    memory, pre-widened to float (fewest instructions per row).
+#ifndef KVR_VEC_SPECIALISE
+#define KVR_VEC_SPECIALISE 1
+#endif
 // Threads per CTA of the shared-memory flavour (its CTAs stage the constants).
 #ifndef KVR_VEC_THREADS
 #define KVR_VEC_THREADS 128
@@ -90,13 +94,16 @@ struct VecShape {
     static constexpr int warps = threads / 32;
 };
 
-template <class IT, int CPL, int CK, bool REG_GAMMA, bool PARAMS_READY>
+// DV / DK: the row split when fixed at compile time (0: from the parameters).
+template <class IT, int CPL, int CK, bool REG_GAMMA, bool PARAMS_READY, int DV = 0, int DK = 0>
 __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : KVR_VEC_MIN_CTAS)
     kv_vec_kernel(const KvParams p) {
+    const int Dv = DV ? DV : p.Dv;
+    const int Dk = DK ? DK : p.Dk;
     constexpr int WARPS = VecShape<REG_GAMMA>::warps;
     constexpr int THREADS = VecShape<REG_GAMMA>::threads;
     extern __shared__ __align__(16) unsigned char smem[];
-    const int nch = p.Dv >> 3;
+    const int nch = Dv >> 3;
     float4* g_lo = reinterpret_cast<float4*>(smem);
     float4* g_hi = g_lo + nch;
     float4* c_lo = g_hi + nch;
@@ -104,7 +111,7 @@ __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : 
     float* s_kscale = reinterpret_cast<float*>(c_hi + nch);
 
     const int lane = threadIdx.x & 31;
-    const int h = p.Dk >> 1;
+    const int h = Dk >> 1;
     const int64_t stride_rows = int64_t(gridDim.x) * WARPS;
     int64_t t = int64_t(blockIdx.x) * WARPS + (threadIdx.x >> 5);
 
@@ -116,11 +123,11 @@ __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : 
     // prefetches measured 2% faster per decode call than bulk prefetches.)
     if (t < p.T) {
         const char* kvrow = static_cast<const char*>(p.kv) + t * p.kv_stride * 2;
-        const int kb = (p.Dv + p.Dk) * 2;
+        const int kb = (Dv + Dk) * 2;
         const int nl = min((kb + 127) / 128 + 1, 29);
         if (lane < nl) prefetch_l2(kvrow + min(lane * 128, kb - 1));
-        else if (lane == 29) prefetch_l2(static_cast<const char*>(p.cos) + t * p.Dk * 2);
-        else if (lane == 30) prefetch_l2(static_cast<const char*>(p.sin) + t * p.Dk * 2);
+        else if (lane == 29) prefetch_l2(static_cast<const char*>(p.cos) + t * Dk * 2);
+        else if (lane == 30) prefetch_l2(static_cast<const char*>(p.sin) + t * Dk * 2);
         else if (lane == 31) prefetch_l2(p.index + index_pos(p, t));
     }
     const bool cper = CK != OUT16 && p.ckv_scale_per_ch;
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : 
             stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, threadIdx.x, THREADS);
             if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, threadIdx.x, THREADS);
             if (kq && p.k_scale_per_ch)
-                for (int i = threadIdx.x; i < p.Dk; i += THREADS) s_kscale[i] = p.k_scale[i];
+                for (int i = threadIdx.x; i < Dk; i += THREADS) s_kscale[i] = p.k_scale[i];
         }
     };
     if constexpr (PARAMS_READY) load_consts();
@@ -153,7 +160,7 @@ __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : 
     pdl_launch_dependents();
     if (REG_GAMMA && t >= p.T) return;
     RowRegs r;
-    if (t < p.T) load_row<CPL>(p, t, lane, nch, h, r);
+    if (t < p.T) load_row<CPL>(p, t, lane, nch, h, Dv, Dk, r);
     if constexpr (!PARAMS_READY) load_consts();
     const float* kscale = (kq && p.k_scale_per_ch) ? (REG_GAMMA ? p.k_scale : s_kscale) : nullptr;
     if constexpr (!REG_GAMMA) __syncthreads();
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : 
             }
             const float ss = warp_sum(acc.x + acc.y);
             const float rr = rsqrtf(fmaf(ss, p.inv_dv, p.eps)) * p.alpha;
-            char* crow = static_cast<char*>(p.ckv) + row * p.Dv * (CK == OUT16 ? 2 : 1);
+            char* crow = static_cast<char*>(p.ckv) + row * Dv * (CK == OUT16 ? 2 : 1);
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const int ch = c * 32 + lane;
@@ -186,20 +193,20 @@ __global__ void __launch_bounds__(VecShape<REG_GAMMA>::threads, REG_GAMMA ? 8 : 
                     chunk_store<IT, CK>(crow + ch * (CK == OUT16 ? 16 : 8), xg[c], rr, cper ? &c_lo[ch] : nullptr,
                                         cper ? &c_hi[ch] : nullptr, cscale0);
             }
-            char* krow = static_cast<char*>(p.kc) + row * p.Dk * (kq ? 1 : 2);
+            char* krow = static_cast<char*>(p.kc) + row * Dk * (kq ? 1 : 2);
             if (lane < h) rope_pair_store<IT>(krow, lane, h, r.xp, r.c0, r.s0, r.c1, r.s1, p.k_kind, kscale, kscale0);
             for (int i = lane + 32; i < h; i += 32) {
                 const char* x = static_cast<const char*>(p.kv) + t * p.kv_stride * 2;
-                const uint16_t* cr = static_cast<const uint16_t*>(p.cos) + t * p.Dk;
-                const uint16_t* sr = static_cast<const uint16_t*>(p.sin) + t * p.Dk;
-                rope_pair_store<IT>(krow, i, h, ld_stream_u32(x + int64_t(p.Dv) * 2 + i * 4), cr[i], sr[i], cr[h + i],
+                const uint16_t* cr = static_cast<const uint16_t*>(p.cos) + t * Dk;
+                const uint16_t* sr = static_cast<const uint16_t*>(p.sin) + t * Dk;
+                rope_pair_store<IT>(krow, i, h, ld_stream_u32(x + int64_t(Dv) * 2 + i * 4), cr[i], sr[i], cr[h + i],
                                     sr[h + i], p.k_kind, kscale, kscale0);
             }
         } else if (row == ROW_BAD && lane == 0 && p.status != nullptr) {
             atomicOr(p.status, KVR_DEVERR_INDEX);
         }
         t += stride_rows;
-        if (t < p.T) load_row<CPL>(p, t, lane, nch, h, r);
+        if (t < p.T) load_row<CPL>(p, t, lane, nch, h, Dv, Dk, r);
     }
 }
 
@@ -264,14 +271,15 @@ __global__ void __launch_bounds__(KV_THREADS) kv_generic_kernel(const KvParams p
 
 typedef void (*VecKernel)(const KvParams);
 
-template <class IT, int CPL, bool PR>
+template <class IT, int CPL, bool PR, int DV = 0, int DK = 0>
 static VecKernel pick_ck(int ck, bool reg_gamma) {
     switch (ck) {
         case OUT16:
-            return reg_gamma ? kv_vec_kernel<IT, CPL, OUT16, true, PR> : kv_vec_kernel<IT, CPL, OUT16, false, PR>;
-        case OUT_I8: return kv_vec_kernel<IT, CPL, OUT_I8, false, PR>;
-        case OUT_E4M3: return kv_vec_kernel<IT, CPL, OUT_E4M3, false, PR>;
-        default: return kv_vec_kernel<IT, CPL, OUT_E5M2, false, PR>;
+            return reg_gamma ? kv_vec_kernel<IT, CPL, OUT16, true, PR, DV, DK>
+                             : kv_vec_kernel<IT, CPL, OUT16, false, PR, DV, DK>;
+        case OUT_I8: return kv_vec_kernel<IT, CPL, OUT_I8, false, PR, DV, DK>;
+        case OUT_E4M3: return kv_vec_kernel<IT, CPL, OUT_E4M3, false, PR, DV, DK>;
+        default: return kv_vec_kernel<IT, CPL, OUT_E5M2, false, PR, DV, DK>;
     }
 }
 
@@ -282,8 +290,12 @@ static VecKernel pick_cpl_pr(int cpl, int ck, bool reg_gamma) {
     return pick_ck<IT, 4, PR>(ck, reg_gamma);
 }
 
+// The MLA latent split (Dv = 512, Dk = 64) is compiled as constants: the
+// chunk bounds tests, the second RoPE loop and the row offsets fold away.
 template <class IT>
-static VecKernel pick_cpl(int cpl, int ck, bool reg_gamma, bool params_ready) {
+static VecKernel pick_cpl(int cpl, int ck, bool reg_gamma, bool params_ready, int Dv, int Dk) {
+    if (KVR_VEC_SPECIALISE && Dv == 512 && Dk == 64)
+        return params_ready ? pick_ck<IT, 2, true, 512, 64>(ck, reg_gamma) : pick_ck<IT, 2, false, 512, 64>(ck, reg_gamma);
     return params_ready ? pick_cpl_pr<IT, true>(cpl, ck, reg_gamma) : pick_cpl_pr<IT, false>(cpl, ck, reg_gamma);
 }
 
@@ -315,8 +327,8 @@ cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, c
         // Register-held gamma for small batches into 16-bit caches (latency),
         // shared-memory constants otherwise (instructions per row).
         const bool reg_gamma = ckv_kind == OUT16 && p.T < KVR_REG_GAMMA_MAX_ROWS;
-        VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind, reg_gamma, p.params_ready != 0)
-                                            : pick_cpl<F16>(cpl, ckv_kind, reg_gamma, p.params_ready != 0);
+        VecKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind, reg_gamma, p.params_ready != 0, p.Dv, p.Dk)
+                                            : pick_cpl<F16>(cpl, ckv_kind, reg_gamma, p.params_ready != 0, p.Dv, p.Dk);
         const size_t smem = reg_gamma ? 0 : size_t(p.Dv) * 8 + size_t(p.Dk) * 4;
         const int threads = reg_gamma ? VecShape<true>::threads : VecShape<false>::threads;
         const int64_t ctas = (p.T + threads / 32 - 1) / (threads / 32);

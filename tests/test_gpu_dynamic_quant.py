@@ -29,7 +29,7 @@ def test_decode_workload_full_size():
     check(q)
 
 
-@pytest.mark.parametrize("H", [512, 8, 24, 1024, 1000, 7, 1, 2048])
+@pytest.mark.parametrize("H", [512, 8, 24, 128, 256, 1024, 1000, 7, 1, 2048])
 def test_shapes(H):
     check(wl.dynamic_quant_decode(seed=H, T=5, heads=7, Hckv=H))
 
