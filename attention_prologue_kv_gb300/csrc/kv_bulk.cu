@@ -48,13 +48,16 @@ constexpr int BULK_THREADS = 32 * (1 + BULK_CONSUMERS);
 #define KVR_BULK_PREFETCH 1
 #endif
 
-template <class IT, int CPL, int CK>
+// DV / DK: the row split when fixed at compile time (0: from the parameters).
+template <class IT, int CPL, int CK, int DV = 0, int DK = 0>
 __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_kernel(const KvParams p) {
+    const int Dv = DV ? DV : p.Dv;
+    const int Dk = DK ? DK : p.Dk;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + p.S;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.S);
-    const int nch = p.Dv >> 3;
+    const int nch = Dv >> 3;
     float4* g_lo = reinterpret_cast<float4*>(smem + p.off_consts);
     float4* g_hi = g_lo + nch;
     float4* c_lo = g_hi + nch;
@@ -65,8 +68,8 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t ntiles = (p.T + p.R - 1) / p.R;
-    const uint32_t kv_row = uint32_t(p.Dv + p.Dk) * 2;
-    const uint32_t cs_row = uint32_t(p.Dk) * 2;
+    const uint32_t kv_row = uint32_t(Dv + Dk) * 2;
+    const uint32_t cs_row = uint32_t(Dk) * 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.S; ++s) {
@@ -134,13 +137,13 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
 
     // ---------------- consumers ----------------
     const int ct = threadIdx.x - 32;
-    const int h = p.Dk >> 1;
+    const int h = Dk >> 1;
     stage_gamma<IT>(g_lo, g_hi, nch, p.gamma, ct, 32 * BULK_CONSUMERS);
     const bool cper = CK != OUT16 && p.ckv_scale_per_ch;
     const bool kq = p.k_kind != OUT16;
     if (cper) stage_chan_f32(c_lo, c_hi, nch, p.ckv_scale, ct, 32 * BULK_CONSUMERS);
     if (kq && p.k_scale_per_ch)
-        for (int i = ct; i < p.Dk; i += 32 * BULK_CONSUMERS) s_kscale[i] = p.k_scale[i];
+        for (int i = ct; i < Dk; i += 32 * BULK_CONSUMERS) s_kscale[i] = p.k_scale[i];
     const float cscale0 = (CK != OUT16 && !p.ckv_scale_per_ch) ? p.ckv_scale[0] : 1.f;
     const float kscale0 = (kq && !p.k_scale_per_ch) ? p.k_scale[0] : 1.f;
     const float* kscale = (kq && p.k_scale_per_ch) ? s_kscale : nullptr;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
             }
             const float ss = warp_sum(acc.x + acc.y);
             const float rr = rsqrtf(fmaf(ss, p.inv_dv, p.eps)) * p.alpha;
-            char* crow = static_cast<char*>(p.ckv) + row * p.Dv * (CK == OUT16 ? 2 : 1);
+            char* crow = static_cast<char*>(p.ckv) + row * Dv * (CK == OUT16 ? 2 : 1);
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const int ch = c * 32 + lane;
@@ -192,10 +195,10 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
                     chunk_store<IT, CK>(crow + ch * (CK == OUT16 ? 16 : 8), xg[c], rr, cper ? &c_lo[ch] : nullptr,
                                         cper ? &c_hi[ch] : nullptr, cscale0);
             }
-            const uint32_t* xp = reinterpret_cast<const uint32_t*>(xr + p.Dv * 2);
-            const uint16_t* cr = reinterpret_cast<const uint16_t*>(st + p.off_cos) + size_t(r) * p.Dk;
-            const uint16_t* sr = reinterpret_cast<const uint16_t*>(st + p.off_sin) + size_t(r) * p.Dk;
-            char* krow = static_cast<char*>(p.kc) + row * p.Dk * (kq ? 1 : 2);
+            const uint32_t* xp = reinterpret_cast<const uint32_t*>(xr + Dv * 2);
+            const uint16_t* cr = reinterpret_cast<const uint16_t*>(st + p.off_cos) + size_t(r) * Dk;
+            const uint16_t* sr = reinterpret_cast<const uint16_t*>(st + p.off_sin) + size_t(r) * Dk;
+            char* krow = static_cast<char*>(p.kc) + row * Dk * (kq ? 1 : 2);
             for (int i = lane; i < h; i += 32)
                 rope_pair_store<IT>(krow, i, h, xp[i], cr[i], sr[i], cr[h + i], sr[h + i], p.k_kind, kscale, kscale0);
         }
@@ -206,18 +209,23 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
 
 typedef void (*BulkKernel)(const KvParams);
 
-template <class IT, int CPL>
+template <class IT, int CPL, int DV = 0, int DK = 0>
 static BulkKernel pick_ck(int ck) {
     switch (ck) {
-        case OUT16: return kv_bulk_kernel<IT, CPL, OUT16>;
-        case OUT_I8: return kv_bulk_kernel<IT, CPL, OUT_I8>;
-        case OUT_E4M3: return kv_bulk_kernel<IT, CPL, OUT_E4M3>;
-        default: return kv_bulk_kernel<IT, CPL, OUT_E5M2>;
+        case OUT16: return kv_bulk_kernel<IT, CPL, OUT16, DV, DK>;
+        case OUT_I8: return kv_bulk_kernel<IT, CPL, OUT_I8, DV, DK>;
+        case OUT_E4M3: return kv_bulk_kernel<IT, CPL, OUT_E4M3, DV, DK>;
+        default: return kv_bulk_kernel<IT, CPL, OUT_E5M2, DV, DK>;
     }
 }
 
+// The MLA latent split (Dv = 512, Dk = 64) is compiled as constants.
+#ifndef KVR_BULK_SPECIALISE
+#define KVR_BULK_SPECIALISE 1
+#endif
 template <class IT>
-static BulkKernel pick_cpl(int cpl, int ck) {
+static BulkKernel pick_cpl(int cpl, int ck, int Dv, int Dk) {
+    if (KVR_BULK_SPECIALISE && Dv == 512 && Dk == 64) return pick_ck<IT, 2, 512, 64>(ck);
     if (cpl == 1) return pick_ck<IT, 1>(ck);
     if (cpl == 2) return pick_ck<IT, 2>(ck);
     return pick_ck<IT, 4>(ck);
@@ -272,7 +280,8 @@ cudaError_t launch_kv_bulk(const KvParams& p0, int in_dtype, int ckv_kind, cudaS
 
     const int nch = p.Dv / 8;
     const int cpl = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
-    BulkKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind) : pick_cpl<F16>(cpl, ckv_kind);
+    BulkKernel fn = in_dtype == KVR_BF16 ? pick_cpl<BF16>(cpl, ckv_kind, p.Dv, p.Dk)
+                                         : pick_cpl<F16>(cpl, ckv_kind, p.Dv, p.Dk);
     cudaError_t e = ensure_smem(fn);
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (p.T + R - 1) / R;
