@@ -193,6 +193,25 @@ class PreparedCall:
             raise KvrError(st, self._name + "_staged")
 
 
+_EMPTY_PAST = {}
+
+
+def _past_ptr(past, device):
+    """Address of past_block_index_keys for the C call. An empty buffer
+    (Bp = 0) still selects the concat-output form, but PyTorch gives it no
+    address and NULL means in place; a small per-device placeholder, never
+    read (Bp = 0), stands in for it."""
+    if past is None:
+        return None
+    if past.numel() > 0:
+        return _ptr(past, "past_block_index_keys")
+    _cuda(past, "past_block_index_keys")
+    key = str(device)
+    if key not in _EMPTY_PAST:
+        _EMPTY_PAST[key] = torch.zeros(8, dtype=torch.int16, device=device)
+    return _EMPTY_PAST[key].data_ptr()
+
+
 def _host_addr(t, name):
     if isinstance(t, int):
         return t
@@ -286,7 +305,7 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
         next_incomplete_raw_keys=_ptr(next_incomplete_raw_keys, "next_incomplete_raw_keys"),
         next_incomplete_rope=_ptr(next_incomplete_rope, "next_incomplete_rope"),
         dev_status=_ptr(dev_status, "dev_status"), rope_layout=N.QSA_ROPE_LAYOUTS[rope_layout],
-        past_block_index_keys=_ptr(past_block_index_keys, "past_block_index_keys"), Bp=Bp)
+        past_block_index_keys=_past_ptr(past_block_index_keys, raw.device), Bp=Bp)
     if block_keys.shape[0] != Nn or block_keys.shape[2] != Di:
         raise ValueError("block_keys must be [N, Bcap, Di]")
     st = N.lib().qsa_prepare(ctypes.byref(a), _stream(stream))

@@ -106,3 +106,43 @@ def test_dynamic_quant_random_configurations(i):
     codes, s = ref_dynamic_quant(q.reshape(-1, H).to(torch.float64).numpy())
     assert np.array_equal(out.cpu().reshape(-1, H).numpy(), codes)
     assert np.array_equal(scale.cpu().reshape(-1).numpy(), s)
+
+
+@pytest.mark.parametrize("i", range(20))
+def test_kv_random_configurations_compiled_split(i):
+    """The same draws with the row split the kernels compile as constants
+    (Dv = 512, Dk = 64): modes, code types, scales, strides, skips, f16 and
+    params_ready still vary."""
+    cfg, params_ready = kv_config(100 + i)
+    cfg.update(Dv=512, Dk=64)
+    case = wl.make_kv_case("fuzz", **cfg)
+    ref_ckv, ref_k, ref_st = run_oracle_kv(case)
+    g_ckv, g_k, g_st = run_gpu_kv(case, params_ready=params_ready)
+    assert g_st == ref_st, cfg
+    n1, _ = compare_cache(g_ckv, ref_ckv, case.ckv_dtype, case.Dv)
+    n2, _ = compare_cache(g_k, ref_k, case.k_dtype, case.Dk)
+    assert n1 == n2 == case.active_tokens(), cfg
+
+
+@pytest.mark.parametrize("i", range(15))
+def test_qsa_random_configurations_compiled_shapes(i):
+    """QSA draws with (Di, kbs) from the compiled set."""
+    cfg, opt = qsa_config(100 + i)
+    r = np.random.default_rng(7500 + i)
+    cfg.update(Di=int(r.choice([64, 128, 256])), kbs=int(r.choice([32, 64, 128])), L=int(r.integers(0, 400)))
+    cfg["Dr"] = min(cfg["Dr"], cfg["Di"]) if cfg["rope"] else 0
+    case = wl.make_qsa_case("fuzz", **cfg)
+    past_bk = None
+    if opt["concat"]:
+        K = case.key_length.expand(case.N) if case.key_length.numel() == 1 else case.key_length
+        Bp = max(0, int(((K - case.L) // case.kbs).max()) + opt["bp_extra"])
+        past_bk = np.random.default_rng(i).integers(0, 0x7C00, (case.N, Bp, case.Di), dtype=np.uint16)
+    kw = dict(carry=opt["carry"], rope_layout=opt["rope_layout"], past_block_keys=past_bk)
+    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, **kw)
+    assert g_st == r_st, (cfg, opt)
+    compare_cache(g_bk, r_bk, "bf16" if cfg["in_dtype"] == "bf16" else "f16", case.Di)
+    if opt["carry"]:
+        assert np.array_equal(g_nr, r_nr, equal_nan=True)
+        if case.Dr:
+            assert np.array_equal(g_npr, r_npr, equal_nan=True)

@@ -249,3 +249,13 @@ def test_compile_time_shape_concat_form():
     case = wl.make_qsa_case("sp", 6, 256, Di=128, Dr=64, kbs=32, seed=78, past_max=700)
     P = np.array(case.meta["past"])
     check(case, past_block_keys=_past_codes(case, int((P // 32).max()) + 2, 79))
+
+
+def test_concat_form_with_an_empty_past_buffer():
+    """Bp = 0 is still the concat-output form: every sequence with past
+    blocks raises KVR_DEVERR_PAST_BLOCKS (an empty tensor has no address,
+    which the C call would otherwise read as in place)."""
+    case = wl.make_qsa_case("e", 3, 40, Di=128, Dr=64, kbs=32, seed=80, past=[0, 40, 70])
+    past = np.zeros((3, 0, 128), dtype=np.uint16)
+    assert run_oracle_qsa(case, past_block_keys=past)[3] == 0x10
+    check(case, past_block_keys=past)
