@@ -48,6 +48,9 @@ cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaSt
 
 // Defined in bounded_wait.cu.
 cudaError_t launch_bounded_wait(int32_t* status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t s);
+// Defined in staging.cu.
+cudaError_t launch_stage_in(void* dst, const void* src, int64_t bytes, cudaStream_t s);
+cudaError_t launch_status_out(int32_t* host_status, const int32_t* dev_status, cudaStream_t s);
 
 }  // namespace kvr
 
@@ -224,6 +227,21 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
     return cuda_status(launch_kv(plan.p, plan.in_dtype, plan.ckv_kind, plan.path, stream));
 }
 
+// Device address of pinned (page-locked, device-mapped) host memory, or NULL
+// for anything else (pageable or unknown memory keeps the copy-engine path).
+static void* mapped_host_ptr(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+#ifndef KVR_STAGE_WITH_KERNELS
+#define KVR_STAGE_WITH_KERNELS 1
+#endif
+
 kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* a, const void* host_src, void* dev_dst, int64_t bytes,
                                         int32_t* host_status, cudaStream_t stream) {
     if (a == nullptr) return KVR_ERR_NULL;
@@ -234,16 +252,33 @@ kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* a, const void* host_s
     bool empty;
     const kvr_status st = kv_plan(a, &plan, &empty);
     if (st != KVR_OK) return st;
+    // Pinned inputs in whole 16-byte units go through a copy kernel chained
+    // with the KV kernel; anything else through a copy-engine operation.
+    const void* src_dev = (KVR_STAGE_WITH_KERNELS && bytes > 0 && bytes % 16 == 0 && aligned(host_src, 16) &&
+                           aligned(dev_dst, 16))
+                              ? mapped_host_ptr(host_src)
+                              : nullptr;
+    int32_t* status_dev = (KVR_STAGE_WITH_KERNELS && host_status != nullptr && aligned(host_status, 4))
+                              ? static_cast<int32_t*>(mapped_host_ptr(host_status))
+                              : nullptr;
     (void)cudaGetLastError();
-    if (bytes > 0 && cudaMemcpyAsync(dev_dst, host_src, size_t(bytes), cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        return KVR_ERR_CUDA;
+    if (bytes > 0) {
+        const cudaError_t e = src_dev != nullptr
+                                  ? launch_stage_in(dev_dst, src_dev, bytes, stream)
+                                  : cudaMemcpyAsync(dev_dst, host_src, size_t(bytes), cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return KVR_ERR_CUDA;
+    }
     if (!empty) {
         const cudaError_t e = launch_kv(plan.p, plan.in_dtype, plan.ckv_kind, plan.path, stream);
         if (e != cudaSuccess) return KVR_ERR_CUDA;
     }
-    if (host_status != nullptr &&
-        cudaMemcpyAsync(host_status, a->dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return KVR_ERR_CUDA;
+    if (host_status != nullptr) {
+        const cudaError_t e =
+            status_dev != nullptr
+                ? launch_status_out(status_dev, a->dev_status, stream)
+                : cudaMemcpyAsync(host_status, a->dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return KVR_ERR_CUDA;
+    }
     return KVR_OK;
 }
 

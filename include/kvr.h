@@ -188,7 +188,10 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);
  * and nothing is enqueued on an error (as kv_rmsnorm_rope_cache; plus
  * KVR_ERR_SHAPE for bytes < 0, KVR_ERR_NULL for a missing copy pointer or a
  * host_status without args->dev_status). A failed enqueue returns
- * KVR_ERR_CUDA (copies enqueued before it stay enqueued).
+ * KVR_ERR_CUDA (copies enqueued before it stay enqueued). Pinned buffers
+ * (reported as host memory with a device address) in whole 16-byte units
+ * are copied by kernels chained with the call (no copy-engine latency);
+ * other memory goes through cudaMemcpyAsync.
  */
 kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* args, const void* host_src, void* dev_dst, int64_t bytes,
                                         int32_t* host_status, cudaStream_t stream);

@@ -269,6 +269,17 @@ def test_staged_call_from_pinned_host_memory():
     compare_cache(codes_of(k), r_k, "bf16", 64)
     with pytest.raises(ValueError):
         call.staged(host[0].clone(), stage, blob)          # not pinned
+    # pageable memory by raw address: staged through a copy-engine operation
+    pageable = host[1].clone().numpy()
+    ckv.view(torch.int16).fill_(wl.SENTINEL16)
+    k.view(torch.int16).fill_(wl.SENTINEL16)
+    dev_status.zero_()
+    call.staged(pageable.ctypes.data, stage.data_ptr(), blob, host_status[0:1].data_ptr())
+    torch.cuda.synchronize()
+    assert int(host_status[0]) == 0x1
+    r_ckv2, r_k2, _ = run_oracle_kv(b)
+    compare_cache(codes_of(ckv), r_ckv2, "bf16", 512)
+    compare_cache(codes_of(k), r_k2, "bf16", 64)
 
 
 def test_benchmark_decode_sets_match_the_oracle():
