@@ -311,8 +311,15 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
     if (!rope && a->next_incomplete_rope != nullptr) return KVR_ERR_NULL;
     const int64_t kbs = a->key_block_size;
     const int64_t nbmax = (a->L + kbs - 1) / kbs;
-    // Past rows copied per CTA in the concat form: about 16 KB.
-    const int64_t copy_rows = a->Di * 2 >= 16384 ? 1 : 16384 / (a->Di * 2);
+    const int64_t Dr = rope ? a->Dr : 0;
+    const bool vec = (a->Di % 8 == 0) && aligned(a->raw_index_keys, 16) && aligned(a->past_incomplete_raw_keys, 16);
+    const bool bulk = vec && (Dr % 8 == 0) && aligned(a->rope_cos, 16) && aligned(a->rope_sin, 16) &&
+                      aligned(a->past_incomplete_rope, 16) && aligned(a->k_norm_weight, 16);
+    const bool warp = bulk && qsa_warp_shape(a->Di, kbs);
+    // Past rows copied per CTA in the concat form: about 16 KB (4 KB per
+    // warp in the warp-per-block kernel).
+    const int64_t copy_bytes = warp ? 4096 : 16384;
+    const int64_t copy_rows = a->Di * 2 >= copy_bytes ? 1 : copy_bytes / (a->Di * 2);
     const int64_t ncopy = concat ? (std::min(a->Bp, a->Bcap) + copy_rows - 1) / copy_rows : 0;
     if (a->N * (nbmax + 1 + ncopy) > 0x7FFFFFFFLL) return KVR_ERR_SHAPE;
     const void* ptrs[] = {a->raw_index_keys, a->block_keys, a->rope_cos, a->rope_sin, a->k_norm_weight,
@@ -322,7 +329,6 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
         if (!aligned(q, 2)) return KVR_ERR_SHAPE;
     if (!aligned(a->key_length, 8)) return KVR_ERR_SHAPE;
 
-    const int64_t Dr = rope ? a->Dr : 0;
     const int64_t nr_bytes = a->N * (kbs - 1) * a->Di * 2;
     const int64_t nrope_bytes = a->N * 2 * Dr * 2;
     const void* ins[] = {a->raw_index_keys, a->block_keys, a->rope_cos, a->rope_sin, a->k_norm_weight,
@@ -367,15 +373,13 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
     p.Dr = int(Dr);
     p.rope_first = a->rope_layout == KVR_QSA_ROPE_INTERLEAVE_FIRST || a->rope_layout == KVR_QSA_ROPE_HALF_FIRST;
     p.rope_half = a->rope_layout == KVR_QSA_ROPE_HALF_LAST || a->rope_layout == KVR_QSA_ROPE_HALF_FIRST;
+    p.params_ready = a->params_ready != 0;
     p.eps = a->eps;
     p.inv_di = 1.0f / float(a->Di);
     p.inv_kbs = 1.0f / float(kbs);
 
-    const bool vec = (a->Di % 8 == 0) && aligned(a->raw_index_keys, 16) && aligned(a->past_incomplete_raw_keys, 16);
-    const bool bulk = vec && (Dr % 8 == 0) && aligned(a->rope_cos, 16) && aligned(a->rope_sin, 16) &&
-                      aligned(a->past_incomplete_rope, 16) && aligned(a->k_norm_weight, 16);
     (void)cudaGetLastError();
-    return cuda_status(launch_qsa(p, a->in_dtype, vec, bulk, stream));
+    return cuda_status(launch_qsa(p, a->in_dtype, vec, bulk, warp, stream));
 }
 
 kvr_status kvr_check_bounded_wait(int32_t* dev_status, int64_t limit_ns, int64_t abort_after_ns,

@@ -274,6 +274,7 @@ struct QsaParams {
     int Di, Dr;
     int rope_first;      // rotate channels [0, Dr) instead of [Di-Dr, Di)
     int rope_half;       // rotate-half pairs (x[i], x[i+Dr/2]) instead of (x[2i], x[2i+1])
+    int params_ready;    // key_length, tables and weight may be read before the dependency wait
     float eps, inv_di, inv_kbs;
 };
 
@@ -287,7 +288,7 @@ struct DqParams {
 // Launch with programmatic stream serialisation allowed: the grid may be
 // scheduled while the previous kernel on the stream drains; its kernels call
 // pdl_wait() before reading global memory (before it they only issue L2
-// prefetches, and, when the caller sets params_ready, read gamma/scales).
+// prefetches, and, when the caller sets params_ready, read the inputs it covers).
 template <typename... Args>
 cudaError_t launch_pdl(void (*fn)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};
@@ -309,7 +310,9 @@ enum KvPath : int { KV_GENERIC = 0, KV_VEC = 1, KV_BULK = 2 };
 // Launchers (host), defined next to their kernels. Return a CUDA error code.
 cudaError_t launch_kv(const KvParams& p, int in_dtype, int ckv_kind, int path, cudaStream_t s);
 cudaError_t launch_kv_bulk(const KvParams& p, int in_dtype, int ckv_kind, cudaStream_t s);
-cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, cudaStream_t s);
+cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, bool warp, cudaStream_t s);
+// Shapes with a compiled warp-per-block QSA kernel.
+bool qsa_warp_shape(int64_t Di, int64_t kbs);
 cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s);
 cudaError_t launch_dq(const DqParams& p, int in_dtype, bool vec, cudaStream_t s);
 

@@ -72,7 +72,7 @@ __device__ __forceinline__ void copy_past_block_keys(const QsaParams& p, int64_t
     char* dst = static_cast<char*>(p.block_keys) + (n * p.Bcap + r0) * row_b;
     const int64_t bytes = (r1 - r0) * row_b;
     if (p.copy_vec) {
-#pragma unroll 4
+#pragma unroll 8
         for (int64_t e = tid; e < (bytes >> 4); e += nthreads)
             reinterpret_cast<uint4*>(dst)[e] = ld_stream_v4(src + 16 * e);
     } else {
@@ -488,6 +488,280 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
     }
 }
 
+// ---------------------------------------------------------------------------
+// Warp variant for the compile-time shapes (DI, KBS): one warp per
+// candidate, QSA_WARP_TASKS independent warps per CTA, no shared-memory
+// staging and no CTA barrier. A call's warps hold few registers and almost
+// no shared memory, so the next call's warps become resident (and issue
+// their L2 prefetches) while this call still runs. Lane (g, c) sums rows
+// g, g+G, ... of 16-byte chunk c straight from global memory; the loads are
+// issued in batches of 16 rows, so a lane keeps up to 16 loads in flight.
+// The G partial rows meet by warp shuffles; the key row is written by the
+// lanes of group 0 as 16-byte stores. Needs Di % 8 == 0, Dr % 8 == 0 and
+// 16-byte aligned bases (as the bulk variant).
+//
+// PR (params_ready): the caller promises that the kernel launched just
+// before does not write key_length, the RoPE tables, past_incomplete_rope
+// or k_norm_weight. The warp then reads key_length, derives its block,
+// loads the block's cos/sin and weight chunk and prefetches exactly the
+// block's rows into L2 before the dependency wait; after the wait only the
+// row loads remain on its path. Outputs and status bits are written after
+// the wait in both forms.
+// ---------------------------------------------------------------------------
+
+#ifndef KVR_QSA_WARP
+#define KVR_QSA_WARP 1
+#endif
+#ifndef KVR_QSA_WARP_TASKS
+#define KVR_QSA_WARP_TASKS 4
+#endif
+constexpr int QSA_WARP_TASKS = KVR_QSA_WARP_TASKS;
+
+// Scalars of sequence n: K = key_length, past length P = K - L, first
+// block j0 = floor(P / KBS) and the number nb of blocks completed by the call.
+struct QsaSeq {
+    int64_t K, P, j0, nb;
+};
+template <int KBS>
+__device__ __forceinline__ QsaSeq qsa_seq(const QsaParams& p, int64_t n) {
+    QsaSeq q;
+    q.K = p.key_length[p.key_length_per_seq ? n : 0];
+    q.P = q.K - p.L;
+    q.j0 = q.P >= 0 ? q.P / KBS : 0;
+    q.nb = q.P >= 0 ? q.K / KBS - q.j0 : 0;
+    return q;
+}
+
+// The first token's cos/sin for chunk c (when it lies in the rotated
+// channels) and the chunk's k_norm_weight.
+template <int DI>
+__device__ __forceinline__ void qsa_chunk_consts(const QsaParams& p, int64_t n, int64_t tok0, int64_t P, int c,
+                                                 uint4& cv, uint4& sv, uint4& wv) {
+    const int base = p.rope_first ? 0 : DI - p.Dr;
+    const int i0 = c * 8 - base;
+    if (p.Dr > 0 && unsigned(i0) < unsigned(p.Dr)) {
+        const uint16_t* cr;
+        const uint16_t* sr;
+        if (tok0 >= P) {
+            cr = static_cast<const uint16_t*>(p.cos) + (n * p.L + (tok0 - P)) * p.Dr;
+            sr = static_cast<const uint16_t*>(p.sin) + (n * p.L + (tok0 - P)) * p.Dr;
+        } else {
+            cr = static_cast<const uint16_t*>(p.past_rope) + n * 2 * p.Dr;
+            sr = cr + p.Dr;
+        }
+        cv = ld_stream_v4(cr + i0);
+        sv = ld_stream_v4(sr + i0);
+    }
+    if (p.w != nullptr) wv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.w) + c * 8);
+}
+
+template <class IT, int DI, int KBS, bool PR>
+__global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_warp_kernel(const QsaParams p) {
+    static_assert(DI % 8 == 0 && DI / 8 <= 32 && 32 % (DI / 8) == 0, "one row must span a power-of-two number of lanes");
+    constexpr int C = DI / 8;              // 16-byte chunks per row
+    constexpr int G = 32 / C;              // row groups per warp
+    static_assert(KBS % G == 0, "block rows must split evenly over the row groups");
+    constexpr int NR = KBS / G;            // rows summed per lane
+    constexpr int RB = NR < 16 ? NR : 16;  // loads in flight per lane
+    static_assert(NR % RB == 0, "row batches must tile the block");
+    __shared__ __align__(16) float u_s[QSA_WARP_TASKS][DI];
+
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int c = lane % C;
+    const int g = lane / C;
+    const uint32_t per_seq = uint32_t(p.nbmax + 1 + p.ncopy);
+    const uint32_t task = blockIdx.x * QSA_WARP_TASKS + wid;
+    const uint32_t n32 = task / per_seq;
+    const bool live = n32 < uint32_t(p.N);   // the last CTA may hold spare warps
+    const int64_t n = n32;
+    const int64_t jl = int64_t(task - n32 * per_seq);
+    const uint16_t* raw = static_cast<const uint16_t*>(p.raw) + n * p.L * DI;
+    const uint16_t* past = static_cast<const uint16_t*>(p.past_raw) + n * (KBS - 1) * DI;
+
+    QsaSeq q = {0, 0, 0, 0};
+    uint4 cv = make_uint4(0, 0, 0, 0), sv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
+    if (live) {
+        if (PR) q = qsa_seq<KBS>(p, n);
+        // Prefetches are only hints, and L2 is the coherence point: they are
+        // safe before the wait even for inputs the preceding grid writes.
+        if (jl > p.nbmax) {
+            // concat-output copy task: its past block-key rows (all rows below
+            // min(Bp, Bcap) that it may copy; with PR exactly those below j0)
+            if (lane == 0 && p.copy_vec) {
+                int64_t lim = min(p.Bp, p.Bcap);
+                if (PR) lim = q.P >= 0 ? min(lim, q.j0) : 0;
+                const int64_t r0 = (jl - p.nbmax - 1) * p.copy_rows;
+                const int64_t r1 = min(r0 + int64_t(p.copy_rows), lim);
+                if (r1 > r0)
+                    prefetch_l2_bulk(static_cast<const uint16_t*>(p.past_bk) + (n * p.Bp + r0) * DI,
+                                     uint32_t(r1 - r0) * DI * 2);
+            }
+        } else if (PR) {
+            if (q.P >= 0 && jl < q.nb && q.j0 + jl < p.Bcap) {
+                // exactly the block's rows, and its constants
+                const int64_t tok0 = (q.j0 + jl) * KBS;
+                const int n_past = tok0 < q.P ? int(q.P - tok0) : 0;
+                if (lane == 0) {
+                    prefetch_l2_bulk(raw + (tok0 + n_past - q.P) * DI, uint32_t(KBS - n_past) * DI * 2);
+                    if (n_past > 0) prefetch_l2_bulk(past, uint32_t(n_past) * DI * 2);
+                }
+                qsa_chunk_consts<DI>(p, n, tok0, q.P, c, cv, sv, wv);
+            }
+        } else if (lane == 0) {
+#if KVR_QSA_RAW_PREFETCH
+            // New-key rows [jl*KBS, (jl+1)*KBS): the block this warp computes
+            // starts P mod KBS rows earlier, but the union over the sequence's
+            // warps covers every row a completed block reads.
+            if (jl < p.nbmax) {
+                const int64_t r0 = jl * KBS;
+                prefetch_l2_bulk(raw + r0 * DI, uint32_t(min(int64_t(KBS), p.L - r0) * DI * 2));
+            }
+#endif
+#if KVR_QSA_KL_PREFETCH
+            if (jl == 0) prefetch_l2(p.key_length + (p.key_length_per_seq ? n : 0));
+#endif
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!live) return;
+    if (!PR) q = qsa_seq<KBS>(p, n);
+
+    const int64_t P = q.P;
+    if (P < 0) {
+        if (jl == 0 && lane == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_KEY_LENGTH);
+        return;
+    }
+    const int64_t F = q.j0 * KBS;              // first token of the incomplete block
+
+    if (jl > p.nbmax) {
+        copy_past_block_keys(p, n, jl - p.nbmax - 1, q.j0, lane, 32);
+        return;
+    }
+    if (jl == p.nbmax) {
+        if (lane == 0) past_block_status(p, q.j0);
+        // carry outputs: the tokens after the last completed block
+        const int64_t Fn = (q.j0 + q.nb) * KBS;
+        const int rem = int(q.K - Fn);
+        if (p.next_raw != nullptr) {
+            uint16_t* dst = static_cast<uint16_t*>(p.next_raw) + n * (KBS - 1) * DI;
+            const bool v16 = (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+            const int per_row = v16 ? C : DI;
+            for (int e = lane; e < rem * per_row; e += 32) {
+                const int r = e / per_row, k = e - r * per_row;
+                const int64_t tok = Fn + r;
+                const uint16_t* src = tok < P ? past + (tok - F) * DI : raw + (tok - P) * DI;
+                if (v16)
+                    reinterpret_cast<uint4*>(dst + int64_t(r) * DI)[k] = reinterpret_cast<const uint4*>(src)[k];
+                else
+                    dst[int64_t(r) * DI + k] = src[k];
+            }
+        }
+        if (p.next_rope != nullptr && p.Dr > 0 && rem > 0) {
+            uint16_t* dst = static_cast<uint16_t*>(p.next_rope) + n * 2 * p.Dr;
+            for (int e = lane; e < 2 * p.Dr; e += 32) {
+                uint16_t v;
+                if (Fn >= P) {
+                    const int64_t row = (n * p.L + (Fn - P)) * p.Dr;
+                    v = e < p.Dr ? static_cast<const uint16_t*>(p.cos)[row + e]
+                                 : static_cast<const uint16_t*>(p.sin)[row + e - p.Dr];
+                } else {
+                    v = static_cast<const uint16_t*>(p.past_rope)[n * 2 * p.Dr + e];
+                }
+                dst[e] = v;
+            }
+        }
+        return;
+    }
+    if (jl >= q.nb) return;
+    const int64_t j = q.j0 + jl;
+    if (j >= p.Bcap) {
+        if (lane == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_BLOCK_CAP);
+        return;
+    }
+    const int64_t tok0 = j * KBS;
+    // Rows r < n_past are carried (past row r: only the first block can hold
+    // them); row r >= n_past is new row (tok0 - P) + r.
+    const int n_past = tok0 < P ? int(P - tok0) : 0;
+    const int64_t off = (tok0 - P) * DI;
+    if (!PR) qsa_chunk_consts<DI>(p, n, tok0, P, c, cv, sv, wv);
+
+    // ---- block sum ----
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int b = 0; b < NR; b += RB) {
+        uint4 v[RB];
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+            const int r = g + G * (b + k);
+            const uint16_t* src = r < n_past ? past + r * DI : raw + (off + int64_t(r) * DI);
+            v[k] = ld_stream_v4(src + c * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+            acc[0] = __fadd2_rn(acc[0], make_float2(IT::lo(v[k].x), IT::hi(v[k].x)));
+            acc[1] = __fadd2_rn(acc[1], make_float2(IT::lo(v[k].y), IT::hi(v[k].y)));
+            acc[2] = __fadd2_rn(acc[2], make_float2(IT::lo(v[k].z), IT::hi(v[k].z)));
+            acc[3] = __fadd2_rn(acc[3], make_float2(IT::lo(v[k].w), IT::hi(v[k].w)));
+        }
+    }
+    float m[8] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y, acc[2].x, acc[2].y, acc[3].x, acc[3].y};
+#pragma unroll
+    for (int o = C; o < 32; o <<= 1)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m[k] += __shfl_xor_sync(0xFFFFFFFFu, m[k], o);
+
+    // ---- mean, optional RMS normalisation (every group holds the whole row) ----
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m[k] *= p.inv_kbs;
+        ss = fmaf(m[k], m[k], ss);
+    }
+    if (p.w != nullptr) {
+#pragma unroll
+        for (int o = 1; o < C; o <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        const float rr = rsqrtf(fmaf(ss, p.inv_di, p.eps));
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[2 * k] = m[2 * k] * rr * IT::lo(ww[k]);
+            m[2 * k + 1] = m[2 * k + 1] * rr * IT::hi(ww[k]);
+        }
+    }
+
+    // ---- rotation of the layout's Dr channels, one rounding, write ----
+    const int base = p.rope_first ? 0 : DI - p.Dr;
+    const int i0 = c * 8 - base;               // table lane of the chunk's first channel
+    float* u = u_s[wid];
+    if (g == 0 && p.Dr > 0) {
+        reinterpret_cast<float4*>(u + c * 8)[0] = make_float4(m[0], m[1], m[2], m[3]);
+        reinterpret_cast<float4*>(u + c * 8)[1] = make_float4(m[4], m[5], m[6], m[7]);
+    }
+    __syncwarp();
+    if (g != 0) return;
+    if (p.Dr > 0 && unsigned(i0) < unsigned(p.Dr)) {
+        const int h = p.Dr >> 1;
+        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + k;
+            int la, lb;
+            rope_pair_lanes(i, h, p.rope_half, la, lb);
+            const float a = u[base + la];
+            const float bb = u[base + lb];
+            const float cs = (k & 1) ? IT::hi(cw[k >> 1]) : IT::lo(cw[k >> 1]);
+            const float sn = (k & 1) ? IT::hi(sw[k >> 1]) : IT::lo(sw[k >> 1]);
+            m[k] = i < h ? a * cs - bb * sn : bb * cs + a * sn;
+        }
+    }
+    uint16_t* out = static_cast<uint16_t*>(p.block_keys) + (n * p.Bcap + j) * DI;
+    reinterpret_cast<uint4*>(out)[c] =
+        make_uint4(IT::pack(m[0], m[1]), IT::pack(m[2], m[3]), IT::pack(m[4], m[5]), IT::pack(m[6], m[7]));
+}
+
 typedef void (*QsaKernel)(const QsaParams);
 
 // Compile-time shapes for common key widths and block sizes (per-block
@@ -501,6 +775,34 @@ static QsaKernel pick_qsa_kbs(int64_t kbs) {
         case 128: return qsa_bulk_kernel<IT, DI, 128>;
         default: return nullptr;
     }
+}
+
+template <class IT, int DI, bool PR>
+static QsaKernel pick_qsa_warp_kbs(int64_t kbs) {
+    switch (kbs) {
+        case 32: return qsa_warp_kernel<IT, DI, 32, PR>;
+        case 64: return qsa_warp_kernel<IT, DI, 64, PR>;
+        case 128: return qsa_warp_kernel<IT, DI, 128, PR>;
+        default: return nullptr;
+    }
+}
+
+template <class IT, bool PR>
+static QsaKernel pick_qsa_warp(int Di, int64_t kbs) {
+    if (Di == 64) return pick_qsa_warp_kbs<IT, 64, PR>(kbs);
+    if (Di == 128) return pick_qsa_warp_kbs<IT, 128, PR>(kbs);
+    if (Di == 256) return pick_qsa_warp_kbs<IT, 256, PR>(kbs);
+    return nullptr;
+}
+
+bool qsa_warp_shape(int64_t Di, int64_t kbs) {
+#if KVR_QSA_WARP
+    return (Di == 64 || Di == 128 || Di == 256) && (kbs == 32 || kbs == 64 || kbs == 128);
+#else
+    (void)Di;
+    (void)kbs;
+    return false;
+#endif
 }
 
 template <class IT>
@@ -523,8 +825,16 @@ static size_t qsa_bulk_smem(const QsaParams& p) {
     return bytes <= 96 * 1024 ? bytes : 0;
 }
 
-cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, cudaStream_t s) {
+cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, bool warp, cudaStream_t s) {
     const int64_t grid = p.N * (p.nbmax + 1 + p.ncopy);
+    if (warp) {
+        const bool bf = in_dtype == KVR_BF16;
+        QsaKernel fn = p.params_ready ? (bf ? pick_qsa_warp<BF16, true>(p.Di, p.kbs) : pick_qsa_warp<F16, true>(p.Di, p.kbs))
+                                      : (bf ? pick_qsa_warp<BF16, false>(p.Di, p.kbs) : pick_qsa_warp<F16, false>(p.Di, p.kbs));
+        if (fn == nullptr) return cudaErrorInvalidValue;
+        return launch_pdl(fn, dim3(unsigned((grid + QSA_WARP_TASKS - 1) / QSA_WARP_TASKS)),
+                          dim3(32 * QSA_WARP_TASKS), 0, s, p);
+    }
     const size_t bsmem = bulk ? qsa_bulk_smem(p) : 0;
     if (bsmem > 0) {
         QsaKernel fn = in_dtype == KVR_BF16 ? pick_qsa_bulk<BF16>(p.Di, p.kbs) : pick_qsa_bulk<F16>(p.Di, p.kbs);

@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 5
+#define KVR_ABI_VERSION 6
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -252,6 +252,19 @@ typedef enum kvr_qsa_rope {
  *                   KVR_DEVERR_PAST_BLOCKS, the missing rows stay untouched),
  *                   so block_keys ends as the past keys followed by the new
  *                   ones. It must not overlap block_keys or the next_* outputs.
+ *   params_ready    0 (default): every input is read after the kernel waits
+ *                   for the preceding kernel on the stream (programmatic
+ *                   dependent launch). Nonzero: the caller promises that the
+ *                   kernel launched immediately before this call on `stream`
+ *                   writes none of key_length, rope_cos, rope_sin,
+ *                   past_incomplete_rope and k_norm_weight (true when
+ *                   sequence lengths come from the scheduler, the tables are
+ *                   precomputed and the weight is a model weight); the kernel
+ *                   for the compiled shapes (Di in {64, 128, 256}, kbs in
+ *                   {32, 64, 128}, 16-byte aligned) then reads them before
+ *                   that wait, so that only the key rows are read after it.
+ *                   Other shapes ignore the flag. Breaking the promise gives
+ *                   stale values.
  *
  * Limits: N, L >= 0; Di >= 1; 0 <= Dr <= Di, Dr even; Bcap >= 1; Bp >= 0.
  * Mean, normalisation and rotation in float32, one rounding to `in_dtype`.
@@ -278,6 +291,7 @@ typedef struct kvr_qsa_args {
     kvr_qsa_rope rope_layout;
     const void* past_block_index_keys;
     int64_t Bp;
+    int32_t params_ready;
 } kvr_qsa_args;
 
 kvr_status qsa_prepare(const kvr_qsa_args* args, cudaStream_t stream);

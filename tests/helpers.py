@@ -157,7 +157,7 @@ def compare_cache(gpu, ref, dtype, D):
 
 
 def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="interleave_last",
-                past_block_keys=None):
+                past_block_keys=None, params_ready=False):
     """past_block_keys: codes [N, Bp, Di] (numpy) for the concat-output form."""
     import attention_prologue_kv_gb300 as kvr
     from attention_prologue_kv_gb300.workloads import SENTINEL16
@@ -177,6 +177,7 @@ def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="int
                     next_incomplete_raw_keys=nr, next_incomplete_rope=npr, dev_status=status,
                     rope_layout=rope_layout,
                     past_block_index_keys=None if past_block_keys is None else
-                    torch.from_numpy(past_block_keys.view(np.int16)).to(dev).view(case.raw.dtype))
+                    torch.from_numpy(past_block_keys.view(np.int16)).to(dev).view(case.raw.dtype),
+                    params_ready=params_ready)
     torch.cuda.synchronize()
     return codes_of(bk), f64(nr), f64(npr), int(status.item())

@@ -66,7 +66,8 @@ def qsa_config(i):
                 in_dtype=str(r.choice(["bf16", "f16"]))), \
         dict(carry=bool(r.random() < 0.7),
              rope_layout=str(r.choice(["interleave_last", "interleave_first", "half_last", "half_first"])),
-             concat=bool(r.random() < 0.4), bp_extra=int(r.integers(-2, 3)))
+             concat=bool(r.random() < 0.4), bp_extra=int(r.integers(-2, 3)),
+             params_ready=bool(r.random() < 0.5))
 
 
 @pytest.mark.parametrize("i", range(30))
@@ -81,7 +82,7 @@ def test_qsa_random_configurations(i):
         past_bk = np.random.default_rng(i).integers(0, 0x7C00, (case.N, Bp, case.Di), dtype=np.uint16)
     kw = dict(carry=opt["carry"], rope_layout=opt["rope_layout"], past_block_keys=past_bk)
     r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
-    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, **kw)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=opt["params_ready"], **kw)
     assert g_st == r_st, (cfg, opt)
     compare_cache(g_bk, r_bk, "bf16" if cfg["in_dtype"] == "bf16" else "f16", case.Di)
     if opt["carry"]:
@@ -124,7 +125,7 @@ def test_kv_random_configurations_compiled_split(i):
     assert n1 == n2 == case.active_tokens(), cfg
 
 
-@pytest.mark.parametrize("i", range(15))
+@pytest.mark.parametrize("i", range(20))
 def test_qsa_random_configurations_compiled_shapes(i):
     """QSA draws with (Di, kbs) from the compiled set."""
     cfg, opt = qsa_config(100 + i)
@@ -139,7 +140,7 @@ def test_qsa_random_configurations_compiled_shapes(i):
         past_bk = np.random.default_rng(i).integers(0, 0x7C00, (case.N, Bp, case.Di), dtype=np.uint16)
     kw = dict(carry=opt["carry"], rope_layout=opt["rope_layout"], past_block_keys=past_bk)
     r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
-    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, **kw)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=opt["params_ready"], **kw)
     assert g_st == r_st, (cfg, opt)
     compare_cache(g_bk, r_bk, "bf16" if cfg["in_dtype"] == "bf16" else "f16", case.Di)
     if opt["carry"]:

@@ -12,10 +12,10 @@ from helpers import compare_cache, run_gpu_qsa, run_oracle_qsa
 pytestmark = pytest.mark.gpu
 
 
-def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None):
+def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None, params_ready=False):
     kw = dict(carry=carry, rope_layout=rope_layout, past_block_keys=past_block_keys)
     r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
-    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, **kw)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=params_ready, **kw)
     assert g_st == r_st
     if past_block_keys is not None:
         # copied past rows are bit-exact copies
@@ -259,3 +259,34 @@ def test_concat_form_with_an_empty_past_buffer():
     past = np.zeros((3, 0, 128), dtype=np.uint16)
     assert run_oracle_qsa(case, past_block_keys=past)[3] == 0x10
     check(case, past_block_keys=past)
+
+
+@pytest.mark.parametrize("Di,kbs", [(64, 128), (128, 64), (256, 32)])
+def test_params_ready(Di, kbs):
+    """params_ready: the compiled-shape kernel reads key_length, the tables
+    and the weight before its dependency wait; results are unchanged (carry
+    outputs on, every RoPE layout family)."""
+    layout = {64: "half_first", 128: "interleave_last", 256: "interleave_first"}[Di]
+    case = wl.make_qsa_case("pr", 5, 333, Di=Di, Dr=min(64, Di), kbs=kbs, seed=Di + kbs + 1, past_max=900)
+    n, _ = check(case, rope_layout=layout, params_ready=True)
+    assert n == case.completed_blocks()
+
+
+def test_params_ready_full_size_and_status():
+    """The workload with params_ready, then a case whose key_length is short
+    of L for one sequence and whose blocks overflow Bcap for another: the
+    status bits are raised after the wait exactly as without the flag."""
+    case = wl.qsa_prepare_workload()
+    n, exact = check(case, params_ready=True)
+    assert n == 32 * 32 and exact > 0.97
+    bad = wl.make_qsa_case("prs", 3, 256, Di=128, Dr=64, kbs=64, seed=91, past=[0, 70, 300], Bcap=6)
+    bad.key_length[0] = 100     # < L: KVR_DEVERR_KEY_LENGTH, sequence skipped
+    assert run_oracle_qsa(bad)[3] == 0x2 | 0x4
+    for ready in (False, True):
+        check(bad, params_ready=ready)   # status bits equal to the oracle's
+
+
+def test_params_ready_concat_form():
+    case = wl.make_qsa_case("prc", 6, 256, Di=128, Dr=64, kbs=64, seed=92, past_max=2000)
+    P = np.array(case.meta["past"])
+    check(case, past_block_keys=_past_codes(case, int((P // 64).max()) + 1, 93), params_ready=True)
