@@ -600,12 +600,15 @@ def run_extras(dev, kvr, wl, flush_buf):
     r["sets"] = "%d input sets" % len(qs)
     out["qsa_prepare"] = r
 
-    # the same sets with the other RoPE layout family, and in the concat-output
-    # form (past block keys [N, Bp, Di] copied into a fresh output first)
+    # the same sets with the other RoPE layout family, with params_ready (the
+    # kernel before does not write key_length, the tables or the weight), and
+    # in the concat-output form (past block keys [N, Bp, Di] copied into a
+    # fresh output first)
     Bp = int(max(max(p_ // q.kbs for p_ in q.meta["past"]) for q in qs))
     past_bk = torch.zeros(q0.N, Bp, q0.Di, dtype=torch.bfloat16, device=dev)
     for name, kw, extra in (
             ("qsa_prepare_half_first", dict(rope_layout="half_first"), lambda q: 0),
+            ("qsa_prepare_params_ready", dict(params_ready=True), lambda q: 0),
             ("qsa_prepare_concat", dict(past_block_index_keys=past_bk),
              lambda q: 2 * q.Di * 2 * sum(min(Bp, p_ // q.kbs) for p_ in q.meta["past"]))):
         calls = []
