@@ -290,3 +290,40 @@ def test_params_ready_concat_form():
     case = wl.make_qsa_case("prc", 6, 256, Di=128, Dr=64, kbs=64, seed=92, past_max=2000)
     P = np.array(case.meta["past"])
     check(case, past_block_keys=_past_codes(case, int((P // 64).max()) + 1, 93), params_ready=True)
+
+
+def test_compiled_shape_unaligned_buffers():
+    """The warp kernel's 2-byte paths: carry outputs and past block keys that
+    start 2 bytes past a 16-byte boundary (the block keys stay aligned)."""
+    import attention_prologue_kv_gb300 as kvr
+    from helpers import codes_of, f64
+    case = wl.make_qsa_case("ua", 3, 200, Di=128, Dr=64, kbs=64, seed=95, past=[10, 130, 300])
+    P = np.array(case.meta["past"])
+    past = _past_codes(case, int((P // 64).max()) + 1, 96)
+    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, carry=True, past_block_keys=past)
+    dev, dt = "cuda", case.raw.dtype
+
+    def off_by_one(codes):
+        flat = torch.from_numpy(np.ascontiguousarray(codes).view(np.int16).reshape(-1)).to(dev)
+        buf = torch.zeros(flat.numel() + 1, dtype=torch.int16, device=dev)
+        buf[1:] = flat
+        return buf[1:].view(dt).view(codes.shape)
+
+    nan_codes = np.full((case.N, 63, 128), 0x7FC0, dtype=np.uint16)
+    nr = off_by_one(nan_codes)
+    assert nr.data_ptr() % 16 == 2
+    pbk = off_by_one(past)
+    npr = torch.full((case.N, 128), float("nan"), dtype=dt, device=dev)
+    bk = torch.full((case.N, case.Bcap, 128), 0x7FBF, dtype=torch.int16, device=dev).view(dt)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d = lambda t: t.to(dev)
+    for ready in (False, True):
+        kvr.qsa_prepare(d(case.raw), bk, d(case.key_length), d(case.rope_cos), d(case.rope_sin),
+                        d(case.k_norm_weight), d(case.past_raw), d(case.past_rope), 64, case.eps,
+                        next_incomplete_raw_keys=nr, next_incomplete_rope=npr, dev_status=st,
+                        past_block_index_keys=pbk, params_ready=ready)
+        torch.cuda.synchronize()
+        assert int(st.item()) == r_st
+        compare_cache(codes_of(bk), r_bk, "bf16", 128)
+        assert np.array_equal(f64(nr), r_nr, equal_nan=True)
+        assert np.array_equal(f64(npr), r_npr, equal_nan=True)
