@@ -15,7 +15,8 @@ replica on its own GPU; the job value sums tokens over ranks and divides by
 the slowest rank's time (weak scaling, no data-path collective).
 
 Printed on rank 0: one JSON line with the metric, the roofline of the kernel,
-the CPU oracle baseline, the end-to-end figure (host buffers, host<->device
+the CPU oracle baseline (one process, and one spawned process per host core
+under "all_cores"), the end-to-end figure (host buffers, host<->device
 copies inside the timed region), clocks sampled during the timed region, and
 the other workloads (prefill, FP8 quantised, QSA prepare) under "extras".
 """
@@ -265,31 +266,79 @@ def time_each(fn, n, flush, stream):
     return statistics.median(ts), min(ts)
 
 
-def cpu_oracle_baseline(budget_s, sets, d0, d1):
-    """The oracle as it stands, on decode batches of the same workload, for
-    about budget_s seconds of single-process CPU time. Returns tokens/s."""
+def _oracle_inputs(sets, n):
+    """The first n decode batches as the oracle's float64 / int64 arrays."""
+    kv = sets["kv"][:n].double().numpy().reshape(n, -1, 1, 576)
+    cos = sets["cos"][:n].double().numpy().reshape(n, -1, 1, 64)
+    sin = sets["sin"][:n].double().numpy().reshape(n, -1, 1, 64)
+    return kv, cos, sin, sets["index"][:n].numpy(), sets["gamma"].double().numpy()
+
+
+def _oracle_loop(budget_s, kv, cos, sin, index, gamma, d0, d1):
+    """The oracle as it stands on decode batches (cycled) for about budget_s
+    seconds: (tokens/s, batches, seconds)."""
     import numpy as np
-    import torch
 
     import oracle
     ckv = np.full((d0, d1, 512), 0x7FBF, dtype=np.uint16)
     kc = np.full((d0, d1, 64), 0x7FBF, dtype=np.uint16)
-    gamma = sets["gamma"].to(torch.float64).numpy()
     n_tok, n_batch = 0, 0
     t0 = time.perf_counter()
     while True:
-        i = n_batch % sets["kv"].shape[0]
-        kv = sets["kv"][i].double().numpy().reshape(1, -1, 576).transpose(1, 0, 2)
-        cos = sets["cos"][i].double().numpy().reshape(-1, 1, 64)
-        sin = sets["sin"][i].double().numpy().reshape(-1, 1, 64)
-        oracle.ref_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, sets["index"][i].numpy(), ckv, kc,
+        i = n_batch % kv.shape[0]
+        oracle.ref_kv_rmsnorm_rope_cache(kv[i], gamma, cos[i], sin[i], index[i], ckv, kc,
                                          Dv=512, mode="PA_BSND", eps=1e-6)
-        n_tok += kv.shape[0]
+        n_tok += kv.shape[1]
         n_batch += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
     return n_tok / el, n_batch, el
+
+
+def cpu_oracle_baseline(budget_s, sets, d0, d1):
+    """The oracle as it stands, on decode batches of the same workload, for
+    about budget_s seconds of single-process CPU time. Returns tokens/s."""
+    return _oracle_loop(budget_s, *_oracle_inputs(sets, min(16, sets["kv"].shape[0])), d0, d1)
+
+
+def _oracle_process(budget_s, inputs, barrier, out):
+    """One process of the all-cores oracle run, timed after every process is
+    ready (so that the timed windows overlap)."""
+    barrier.wait(timeout=600)
+    out.put(_oracle_loop(budget_s, *inputs))
+
+
+def cpu_oracle_all_cores(budget_s, sets, d0, d1, n=None):
+    """The same oracle in one process per host core (n processes if given;
+    spawned, so no process inherits a CUDA context; each gets its own decode
+    batches), started together: aggregate tokens/s."""
+    import multiprocessing as mp
+    n = n or os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    barrier, out = ctx.Barrier(n), ctx.Queue()
+    kv, cos, sin, index, gamma = _oracle_inputs(sets, min(16, sets["kv"].shape[0]))
+    procs = []
+    for i in range(n):
+        j = [i % kv.shape[0]]
+        procs.append(ctx.Process(target=_oracle_process,
+                                 args=(budget_s, (kv[j], cos[j], sin[j], index[j], gamma, d0, d1), barrier, out)))
+    for p in procs:
+        p.start()
+    res, deadline = [], time.time() + 600
+    while len(res) < n and time.time() < deadline:
+        try:
+            res.append(out.get(timeout=1.0))
+        except Exception:   # queue.Empty: check that no process has failed
+            if any(p.exitcode not in (None, 0) for p in procs):
+                break
+    for p in procs:
+        p.join(timeout=5)
+        if p.is_alive():
+            p.terminate()
+    if len(res) < n:
+        return None
+    return sum(r[0] for r in res), n, sum(r[1] for r in res), max(r[2] for r in res)
 
 
 def run_ours(args):
@@ -397,6 +446,7 @@ def run_ours(args):
         e2e = e2e_decode(args, sets, gamma, ckv, kc, dev, kvr)
         extras = None if args.no_extras else run_extras(dev, kvr, wl, flush_buf)
         cpu_tps, n_batches, cpu_s = cpu_oracle_baseline(args.cpu_seconds, sets, d0, d1)
+        all_cores = cpu_oracle_all_cores(max(1.0, args.cpu_seconds / 2), sets, d0, d1)
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": job_ms / K, "higher_is_better": True,
@@ -416,7 +466,11 @@ def run_ours(args):
                          "traffic_source": PROFILE_SUMMARY.replace(ROOT + "/", "") if traffic else traffic_state},
             "cpu_baseline": {"value": cpu_tps, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": "%d decode batches of 256 tokens (%.1f s, float64 NumPy, one process)"
-                                       % (n_batches, cpu_s)},
+                                       % (n_batches, cpu_s),
+                             "all_cores": None if all_cores is None else {
+                                 "value": all_cores[0], "unit": UNIT, "cores": all_cores[1],
+                                 "sample": "%d processes (one per host core, spawned, started together), "
+                                           "%d decode batches of 256 tokens in %.1f s" % all_cores[1:]}},
             "e2e": e2e,
             "gpu_launches": K,
             "clocks": clocks,

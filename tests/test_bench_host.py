@@ -67,3 +67,17 @@ def test_kernel_source_hash_ignores_comments_not_code():
     assert bench._code_tokens(a) == bench._code_tokens(b)
     assert bench._code_tokens(a) != bench._code_tokens(a.replace("x = 1", "x = 2"))
     assert bench._code_tokens(a) != bench._code_tokens(a.replace("mov //", "mov2 //"))
+
+
+def test_cpu_baseline_on_several_processes():
+    """The oracle baseline in spawned processes (one per host core in the
+    benchmark; two here): every process reports, the aggregate counts all of
+    them, and each process's rate is of the order of the single-process rate."""
+    from attention_prologue_kv_gb300 import workloads as wl
+    sets = wl.decode_paged_sets(2, seed=1002)
+    one = bench.cpu_oracle_baseline(0.5, sets, sets["d0"], sets["d1"])
+    res = bench.cpu_oracle_all_cores(0.5, sets, sets["d0"], sets["d1"], n=2)
+    assert res is not None
+    tps, procs, batches, secs = res
+    assert procs == 2 and batches >= 2 and secs >= 0.5
+    assert 0.1 * one[0] < tps / procs < 10 * one[0]
