@@ -271,11 +271,14 @@ __global__ void __launch_bounds__(KV_THREADS) kv_generic_kernel(const KvParams p
 
 typedef void (*VecKernel)(const KvParams);
 
+// The register-gamma flavour ignores params_ready (the flag permits early
+// reads, it does not require them): reading gamma before the dependency wait
+// made a back-to-back decode call slower (1.76 vs 1.51 us).
 template <class IT, int CPL, bool PR, int DV = 0, int DK = 0>
 static VecKernel pick_ck(int ck, bool reg_gamma) {
     switch (ck) {
         case OUT16:
-            return reg_gamma ? kv_vec_kernel<IT, CPL, OUT16, true, PR, DV, DK>
+            return reg_gamma ? kv_vec_kernel<IT, CPL, OUT16, true, false, DV, DK>
                              : kv_vec_kernel<IT, CPL, OUT16, false, PR, DV, DK>;
         case OUT_I8: return kv_vec_kernel<IT, CPL, OUT_I8, false, PR, DV, DK>;
         case OUT_E4M3: return kv_vec_kernel<IT, CPL, OUT_E4M3, false, PR, DV, DK>;

@@ -142,7 +142,9 @@ typedef enum kvr_cache_mode {
  *              immediately before this call on `stream` does not write gamma,
  *              ckv_scale or k_scale (true of model weights and calibrated
  *              scales); they may then be read before that wait, overlapping
- *              the preceding kernel. Breaking the promise gives stale values.
+ *              the preceding kernel (the small-batch kernel for 16-bit caches
+ *              does not, as that measured slower). Breaking the promise gives
+ *              stale values.
  *
  * Limits: Dv >= 1, Dk >= 2 and even, Bkv, Skv >= 0, d0, d1 >= 1.
  * All arithmetic is float32 with one rounding to the cache type.
