@@ -7,4 +7,5 @@ build step and the seeded synthetic workloads. There is no CPU fallback:
 calling an entry point without the built library raises.
 """
 from .api import (KvrError, PreparedCall, check_bounded_wait, device_copy,  # noqa: E402,F401
-                  dynamic_quant, kv_rmsnorm_rope_cache, prepare_kv_rmsnorm_rope_cache, qsa_prepare)
+                  dynamic_quant, kv_rmsnorm_rope_cache, prepare_kv_rmsnorm_rope_cache, qsa_prepare,
+                  set_debug_validate)

@@ -317,6 +317,16 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
         raise KvrError(st, "qsa_prepare")
 
 
+def set_debug_validate(on):
+    """Debug validation of kv_rmsnorm_rope_cache's index (off by default, or
+    on from the start with KVR_DEBUG_VALIDATE=1): each call then copies its
+    index to the host, synchronising its stream, and raises KvrError
+    (KVR_ERR_INDEX) without launching when an entry is out of range or two
+    tokens name the same cache row. Calls under CUDA-graph capture are not
+    checked. Slow: for debugging only."""
+    N.lib().kvr_set_debug_validate(1 if on else 0)
+
+
 def check_bounded_wait(dev_status, limit_us, abort_after_us=0, stream=None):
     """Failure-detection check: a kernel waits for an mbarrier phase that
     never completes and gives up after `limit_us` microseconds (or when a

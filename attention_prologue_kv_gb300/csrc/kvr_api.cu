@@ -1,7 +1,11 @@
 // Host side of libkvr.so: argument validation, kernel selection, launch.
 // Every entry point returns before launching anything when its arguments
 // are invalid; see include/kvr.h for the contract.
+#include <atomic>
+#include <cstdlib>
 #include <mutex>
+#include <unordered_set>
+#include <vector>
 
 #include <algorithm>
 
@@ -86,6 +90,83 @@ bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
 }
 
 kvr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVR_OK : KVR_ERR_CUDA; }
+
+// Debug validation: -1 until the environment (KVR_DEBUG_VALIDATE=1) has
+// been read, then 0 or 1; kvr_set_debug_validate() overrides it.
+std::atomic<int> g_debug_validate{-1};
+
+bool debug_validate() {
+    int v = g_debug_validate.load();
+    if (v < 0) {
+        const char* e = std::getenv("KVR_DEBUG_VALIDATE");
+        int unset = -1;
+        g_debug_validate.compare_exchange_strong(unset, (e != nullptr && e[0] == '1') ? 1 : 0);
+        v = g_debug_validate.load();
+    }
+    return v == 1;
+}
+
+// The cache row of every token of a kv_rmsnorm_rope_cache call, read from a
+// host copy of its index: what the kernels cannot check (they see one row
+// at a time) is that no two tokens name the same cache row, which the index
+// restrictions of "aclnnKvRmsNormRopeCache" forbid (within a batch in Norm
+// mode, anywhere in the paged modes). Out-of-range entries are reported
+// here too. Returns KVR_ERR_INDEX on a violation.
+kvr_status check_index_host(const kvr_kv_args* a, const int64_t* idx) {
+    const int64_t Bkv = a->Bkv, Skv = a->Skv, d0 = a->cache_d0, d1 = a->cache_d1;
+    std::unordered_set<int64_t> rows;
+    rows.reserve(size_t(Bkv * Skv));
+    if (a->mode == KVR_CACHE_NORM) {
+        for (int64_t b = 0; b < Bkv; ++b)
+            for (int64_t s = 0; s < Skv; ++s) {
+                const int64_t e = idx[b * Skv + s];
+                if (e == -1) continue;
+                if (e < 0 || e >= d1) return KVR_ERR_INDEX;
+                if (!rows.insert(b * d1 + e).second) return KVR_ERR_INDEX;
+            }
+    } else if (a->mode == KVR_CACHE_PA_BSND) {
+        for (int64_t t = 0; t < Bkv * Skv; ++t) {
+            const int64_t e = idx[t];
+            if (e == -1) continue;
+            if (e < 0 || e >= d0 * d1) return KVR_ERR_INDEX;
+            if (!rows.insert(e).second) return KVR_ERR_INDEX;
+        }
+    } else {   // PA_BLK_BSND: one entry per d1 tokens; token s -> entry + s mod d1, inside the entry's block
+        const int64_t nblk = (Skv + d1 - 1) / d1;
+        for (int64_t b = 0; b < Bkv; ++b)
+            for (int64_t q = 0; q < nblk; ++q) {
+                const int64_t e = idx[b * nblk + q];
+                if (e == -1) continue;
+                const int64_t ntok = std::min(d1, Skv - q * d1);
+                if (e < 0 || e >= d0 * d1 || e % d1 + ntok > d1) return KVR_ERR_INDEX;
+                for (int64_t r = 0; r < ntok; ++r)
+                    if (!rows.insert(e + r).second) return KVR_ERR_INDEX;
+            }
+    }
+    return KVR_OK;
+}
+
+// Copy the index of a planned call to the host (synchronising `stream`) and
+// check it. Skipped while the stream is being captured into a graph (a
+// capture cannot synchronise).
+kvr_status debug_check_index(const kvr_kv_args* a, cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KVR_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return KVR_OK;
+    const int64_t nblk = (a->Skv + a->cache_d1 - 1) / a->cache_d1;
+    const int64_t n = a->mode == KVR_CACHE_PA_BLK_BSND ? a->Bkv * nblk : a->Bkv * a->Skv;
+    std::vector<int64_t> idx(static_cast<size_t>(n));
+    if (cudaMemcpyAsync(idx.data(), a->index, size_t(n) * sizeof(int64_t), cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KVR_ERR_CUDA;
+    }
+    return check_index_host(a, idx.data());
+}
 
 }  // namespace
 
@@ -214,15 +295,22 @@ const char* kvr_status_string(kvr_status s) {
         case KVR_ERR_MODE: return "unknown cache mode";
         case KVR_ERR_ALIAS: return "an output overlaps an input it must not overlap";
         case KVR_ERR_CUDA: return "the CUDA launch failed";
+        case KVR_ERR_INDEX: return "debug validation: an index entry is out of range or names a cache row another entry names";
     }
     return "unknown status";
 }
+
+void kvr_set_debug_validate(int on) { g_debug_validate.store(on ? 1 : 0); }
 
 kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* a, cudaStream_t stream) {
     KvPlan plan;
     bool empty;
     const kvr_status st = kv_plan(a, &plan, &empty);
     if (st != KVR_OK || empty) return st;
+    if (debug_validate()) {
+        const kvr_status v = debug_check_index(a, stream);
+        if (v != KVR_OK) return v;
+    }
     (void)cudaGetLastError();
     return cuda_status(launch_kv(plan.p, plan.in_dtype, plan.ckv_kind, plan.path, stream));
 }
@@ -267,6 +355,10 @@ kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* a, const void* host_s
                                   ? launch_stage_in(dev_dst, src_dev, bytes, stream)
                                   : cudaMemcpyAsync(dev_dst, host_src, size_t(bytes), cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return KVR_ERR_CUDA;
+    }
+    if (!empty && debug_validate()) {   // after the copy: the index may be part of the staged inputs
+        const kvr_status v = debug_check_index(a, stream);
+        if (v != KVR_OK) return v;
     }
     if (!empty) {
         const cudaError_t e = launch_kv(plan.p, plan.in_dtype, plan.ckv_kind, plan.path, stream);

@@ -28,11 +28,12 @@
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller (the
  *     host-staged entry point also takes pinned host buffers); the library
- *     allocates nothing and keeps no per-call state. Rows are dense and
- *     row-major unless a stride argument says otherwise.
+ *     allocates no device memory and keeps no per-call state. Rows are dense
+ *     and row-major unless a stride argument says otherwise.
  *   - Calls are asynchronous on `stream`: they validate on the host, launch,
  *     and return. Nothing is read back to the host (except the status word
- *     the host-staged entry point copies back, asynchronously).
+ *     the host-staged entry point copies back, asynchronously, and the index
+ *     that the opt-in debug validation, kvr_set_debug_validate, checks).
  *   - Host-side errors (a NULL that is required, a bad shape, dtype or
  *     mode) are returned before any launch; nothing is written.
  *   - Data-dependent errors are found on the device: the offending row or
@@ -66,7 +67,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 6
+#define KVR_ABI_VERSION 7
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -75,7 +76,10 @@ typedef enum kvr_status {
     KVR_ERR_DTYPE = 3,        /* an element type is not supported for that argument */
     KVR_ERR_MODE = 4,         /* unknown cache mode */
     KVR_ERR_ALIAS = 5,        /* an output overlaps an input it must not overlap */
-    KVR_ERR_CUDA = 6          /* the launch failed (see cudaGetLastError) */
+    KVR_ERR_CUDA = 6,         /* the launch failed (see cudaGetLastError) */
+    KVR_ERR_INDEX = 7         /* debug validation only (kvr_set_debug_validate): an index
+                                 entry is out of range or names a cache row that another
+                                 entry of the call names */
 } kvr_status;
 
 /* Bits OR-ed into *dev_status by the kernels. */
@@ -341,6 +345,21 @@ kvr_status kvr_device_copy(void* dst, const void* src, int64_t bytes, cudaStream
  * device word *dev_status and returns: nothing traps and the context stays
  * usable. Asynchronous on `stream`. */
 kvr_status kvr_check_bounded_wait(int32_t* dev_status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t stream);
+
+/* Debug validation of kv_rmsnorm_rope_cache's index (off by default; the
+ * environment variable KVR_DEBUG_VALIDATE=1 turns it on at the first call,
+ * this call sets it either way, for every thread). When on, each
+ * kv_rmsnorm_rope_cache / kv_rmsnorm_rope_cache_staged call copies its index
+ * to the host, synchronising `stream`, and returns KVR_ERR_INDEX without
+ * launching when an entry is out of range or two tokens name the same cache
+ * row ("aclnnKvRmsNormRopeCache", "Restrictions on index": distinct within a
+ * batch in Norm mode, anywhere in the paged modes; in PA_BLK_BSND every
+ * token's row is checked and must stay inside its entry's block). Without
+ * it, repeated rows leave an unspecified winner and out-of-range entries are
+ * skipped and reported through dev_status. A call made while its stream is
+ * being captured into a CUDA graph is not checked. For debugging only: the
+ * copy and the synchronisation cost far more than the call. */
+void kvr_set_debug_validate(int on);
 
 /* Static description of a status code (never NULL). */
 const char* kvr_status_string(kvr_status status);
