@@ -112,13 +112,46 @@ def sentinel_cache(shape, dtype, dev="cuda"):
     return torch.full(shape, sentinel(dtype), dtype=code_torch_dtype(dtype), device=dev).view(TORCH_DTYPES[dtype])
 
 
+GUARD_BYTES = 8192      # guard band before and after every output buffer the kernels write
+GUARD_BYTE = 0x5A       # its fill, checked byte for byte after the call
+
+
+def guarded(shape, dtype, fill, dev="cuda"):
+    """An output buffer of `shape` and torch `dtype` filled with `fill`, placed
+    between two GUARD_BYTES guard bands inside one allocation (16-byte
+    alignment kept). Returns (view, check); check() asserts that no byte of
+    either band changed, i.e. that nothing was written outside the buffer."""
+    esz = torch.empty(0, dtype=dtype).element_size()
+    n = 1
+    for d in shape:
+        n *= int(d)
+    raw = torch.full((GUARD_BYTES * 2 + n * esz,), GUARD_BYTE, dtype=torch.uint8, device=dev)
+    view = raw[GUARD_BYTES:GUARD_BYTES + n * esz].view(dtype).view(shape)
+    view.fill_(fill)
+
+    def check():
+        lo, hi = raw[:GUARD_BYTES], raw[GUARD_BYTES + n * esz:]
+        assert bool(torch.all(lo == GUARD_BYTE)) and bool(torch.all(hi == GUARD_BYTE)), \
+            "a kernel wrote outside its output buffer (guard band changed)"
+    return view, check
+
+
+def guarded_cache(shape, dtype, dev="cuda"):
+    """sentinel_cache between guard bands: (view, check)."""
+    from attention_prologue_kv_gb300.workloads import TORCH_DTYPES, code_torch_dtype, sentinel
+    v, check = guarded(shape, code_torch_dtype(dtype), sentinel(dtype), dev)
+    return v.view(TORCH_DTYPES[dtype]), check
+
+
 def run_gpu_kv(case, kv=None, ckv=None, k=None, dev="cuda", params_ready=False):
     """Run the CUDA path on a KVCase; returns (ckv codes, k codes, status) as numpy/int."""
     import attention_prologue_kv_gb300 as kvr
     sh_ckv, sh_k = case.cache_shapes()
+    checks = []
     if ckv is None:
-        ckv = sentinel_cache(sh_ckv, case.ckv_dtype, dev)
-        k = sentinel_cache(sh_k, case.k_dtype, dev)
+        ckv, c1 = guarded_cache(sh_ckv, case.ckv_dtype, dev)
+        k, c2 = guarded_cache(sh_k, case.k_dtype, dev)
+        checks = [c1, c2]
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kvr.kv_rmsnorm_rope_cache(
         kv_to_device(case, dev) if kv is None else kv, case.gamma.to(dev), case.cos.to(dev),
@@ -127,6 +160,8 @@ def run_gpu_kv(case, kv=None, ckv=None, k=None, dev="cuda", params_ready=False):
         k_scale=None if case.k_scale is None else case.k_scale.to(dev),
         kc_scale=case.kc_scale, dev_status=status, params_ready=params_ready)
     torch.cuda.synchronize()
+    for c in checks:
+        c()
     return codes_of(ckv), codes_of(k), int(status.item())
 
 
@@ -162,14 +197,18 @@ def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="int
     import attention_prologue_kv_gb300 as kvr
     from attention_prologue_kv_gb300.workloads import SENTINEL16
     bk = block_keys
+    checks = []
     if bk is None:
-        bk = torch.full((case.N, case.Bcap, case.Di), SENTINEL16, dtype=torch.int16,
-                        device=dev).view(case.raw.dtype)
+        bk, c = guarded((case.N, case.Bcap, case.Di), torch.int16, SENTINEL16, dev)
+        bk = bk.view(case.raw.dtype)
+        checks.append(c)
     nr = npr = None
     if carry:
-        nr = torch.full((case.N, case.kbs - 1, case.Di), float("nan"), dtype=case.raw.dtype, device=dev)
+        nr, c = guarded((case.N, case.kbs - 1, case.Di), case.raw.dtype, float("nan"), dev)
+        checks.append(c)
         if case.Dr:
-            npr = torch.full((case.N, 2 * case.Dr), float("nan"), dtype=case.raw.dtype, device=dev)
+            npr, c = guarded((case.N, 2 * case.Dr), case.raw.dtype, float("nan"), dev)
+            checks.append(c)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     d = lambda t: None if t is None else t.to(dev)
     kvr.qsa_prepare(d(case.raw), bk, d(case.key_length), d(case.rope_cos), d(case.rope_sin),
@@ -180,4 +219,6 @@ def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="int
                     torch.from_numpy(past_block_keys.view(np.int16)).to(dev).view(case.raw.dtype),
                     params_ready=params_ready)
     torch.cuda.synchronize()
+    for c in checks:
+        c()
     return codes_of(bk), f64(nr), f64(npr), int(status.item())

@@ -6,6 +6,7 @@ import torch
 
 import attention_prologue_kv_gb300 as kvr
 from attention_prologue_kv_gb300 import workloads as wl
+from helpers import guarded
 from oracle.dynamic_quant import ref_dynamic_quant
 
 pytestmark = pytest.mark.gpu
@@ -14,10 +15,12 @@ pytestmark = pytest.mark.gpu
 def check(q_cpu, q_dev=None):
     q_dev = q_cpu.cuda() if q_dev is None else q_dev
     H = q_cpu.shape[-1]
-    out = torch.full(q_cpu.shape, 99, dtype=torch.int8, device="cuda")
-    scale = torch.full(q_cpu.shape[:-1] + (1,), -1.0, dtype=torch.float32, device="cuda")
+    out, c1 = guarded(tuple(q_cpu.shape), torch.int8, 99)
+    scale, c2 = guarded(tuple(q_cpu.shape[:-1]) + (1,), torch.float32, -1.0)
     kvr.dynamic_quant(q_dev, out, scale)
     torch.cuda.synchronize()
+    c1()
+    c2()
     codes, s = ref_dynamic_quant(q_cpu.reshape(-1, H).to(torch.float64).numpy())
     assert np.array_equal(out.cpu().reshape(-1, H).numpy(), codes)
     assert np.array_equal(scale.cpu().reshape(-1).numpy(), s)
