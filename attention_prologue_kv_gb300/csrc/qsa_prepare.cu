@@ -11,10 +11,13 @@
 // channels and rotate-half pairs on request). In the concat-output form the
 // past block keys are copied from past_block_index_keys first.
 //
-// Design: one CTA per (sequence, candidate block); the CTA reads key_length
-// on the device, derives the past length P = K - L, and exits at once if its
-// block is not completed by this call (no host sync). Two variants:
-//  * qsa_bulk_kernel (16-byte-aligned shapes up to 96 KB of rows): 128
+// Design: one warp or CTA per (sequence, candidate block); it reads
+// key_length on the device, derives the past length P = K - L, and exits at
+// once if its block is not completed by this call (no host sync). Three
+// variants:
+//  * qsa_warp_kernel (Di in {64, 128, 256}, kbs in {32, 64, 128}, 16-byte
+//    aligned; described at its definition): one warp per candidate;
+//  * qsa_bulk_kernel (other 16-byte-aligned shapes up to 96 KB of rows): 128
 //    threads; before the dependency wait the CTA prefetches its slice of
 //    new keys into L2; after it, thread 0 reads key_length, derives the
 //    block's scalars once and pulls the block's rows, its first token's
@@ -22,11 +25,11 @@
 //    mbarrier; the CTA then sums the rows from shared memory;
 //  * qsa_kernel (any shape): 256 threads, each keeping kbs/G independent
 //    loads of a (row group g, channel chunk c) slice in flight.
-// Both reduce the G partial rows in shared memory, then take the mean, the
-// block-wide sum of squares, the rotation and one rounding to the output
-// type; the 2*Di-byte key row is written once. One extra CTA per sequence
-// writes the optional carry outputs, and in the concat-output form `ncopy`
-// more CTAs per sequence copy its past block-key rows.
+// The CTA variants reduce the G partial rows in shared memory (the warp
+// variant by shuffles), then take the mean, the sum of squares, the rotation
+// and one rounding to the output type; the 2*Di-byte key row is written
+// once. One extra CTA (warp) per sequence writes the optional carry outputs,
+// and in the concat-output form `ncopy` more copy its past block-key rows.
 #include <mutex>
 #include <set>
 
@@ -255,9 +258,6 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 #ifndef KVR_QSA_RAW_PREFETCH
 #define KVR_QSA_RAW_PREFETCH 1
 #endif
-#ifndef KVR_QSA_SPECIALISE
-#define KVR_QSA_SPECIALISE 1
-#endif
 #ifndef KVR_QSA_KL_PREFETCH
 #define KVR_QSA_KL_PREFETCH 1
 #endif
@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(QSA_THREADS) qsa_kernel(const QsaParams p) {
 constexpr int QSA_BULK_THREADS = KVR_QSA_BULK_THREADS;
 
 // DI / KBS: the key width and block size when fixed at compile time (0: read
-// from the parameters); a fixed shape turns the divisions, modulos and loop
-// bounds that depend on them into constants.
+// from the parameters). Only the runtime-shape form is instantiated: the
+// compiled shapes take the warp kernel below.
 template <class IT, int DI, int KBS>
 __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -762,19 +762,9 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
 
 typedef void (*QsaKernel)(const QsaParams);
 
-// Compile-time shapes for common key widths and block sizes (per-block
-// instruction count is what bounds a small call: 4.85 vs 5.92 us on the
-// 32 x 2048-token workload); any other shape takes the runtime-shape kernel.
-template <class IT, int DI>
-static QsaKernel pick_qsa_kbs(int64_t kbs) {
-    switch (kbs) {
-        case 32: return qsa_bulk_kernel<IT, DI, 32>;
-        case 64: return qsa_bulk_kernel<IT, DI, 64>;
-        case 128: return qsa_bulk_kernel<IT, DI, 128>;
-        default: return nullptr;
-    }
-}
-
+// Compile-time shapes for common key widths and block sizes take the warp
+// kernel (with the sizes as constants, a small call's per-block instruction
+// chain is shorter); any other aligned shape takes the bulk kernel.
 template <class IT, int DI, bool PR>
 static QsaKernel pick_qsa_warp_kbs(int64_t kbs) {
     switch (kbs) {
@@ -803,16 +793,6 @@ bool qsa_warp_shape(int64_t Di, int64_t kbs) {
 #endif
 }
 
-template <class IT>
-static QsaKernel pick_qsa_bulk(int Di, int64_t kbs) {
-    QsaKernel fn = nullptr;
-#if KVR_QSA_SPECIALISE
-    if (Di == 64) fn = pick_qsa_kbs<IT, 64>(kbs);
-    else if (Di == 128) fn = pick_qsa_kbs<IT, 128>(kbs);
-    else if (Di == 256) fn = pick_qsa_kbs<IT, 256>(kbs);
-#endif
-    return fn != nullptr ? fn : qsa_bulk_kernel<IT, 0, 0>;
-}
 
 // Shared memory the bulk variant needs (0 if it does not fit).
 static size_t qsa_bulk_smem(const QsaParams& p) {
@@ -835,7 +815,7 @@ cudaError_t launch_qsa(const QsaParams& p, int in_dtype, bool vec, bool bulk, bo
     }
     const size_t bsmem = bulk ? qsa_bulk_smem(p) : 0;
     if (bsmem > 0) {
-        QsaKernel fn = in_dtype == KVR_BF16 ? pick_qsa_bulk<BF16>(p.Di, p.kbs) : pick_qsa_bulk<F16>(p.Di, p.kbs);
+        QsaKernel fn = in_dtype == KVR_BF16 ? qsa_bulk_kernel<BF16, 0, 0> : qsa_bulk_kernel<F16, 0, 0>;
         if (bsmem > 48 * 1024) {
             static std::mutex mu;
             static std::set<const void*> done;
