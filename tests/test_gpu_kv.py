@@ -282,6 +282,44 @@ def test_staged_call_from_pinned_host_memory():
     compare_cache(codes_of(k), r_k2, "bf16", 64)
 
 
+def test_staged_large_batch():
+    """A 5.8 MB staged input (4096 tokens): more 16-byte elements than the
+    copy kernel has threads, so its grid-stride loop runs several rounds;
+    three steps in a row through one staging buffer."""
+    import attention_prologue_kv_gb300 as kvr
+    from helpers import codes_of
+    cases = [wl.make_kv_case("sl", 64, 64, mode="PA_BSND", d0=512, d1=128, seed=70 + i, skip=9) for i in range(3)]
+    parts = lambda c: [c.kv.reshape(-1).view(torch.uint8), c.cos.reshape(-1).view(torch.uint8),
+                       c.sin.reshape(-1).view(torch.uint8), c.index.reshape(-1).view(torch.uint8)]
+    sizes = [t.numel() for t in parts(cases[0])]
+    blob = sum(sizes)
+    assert blob // 16 > 4 * 304 * 256
+    host = torch.empty(len(cases), blob, dtype=torch.uint8).pin_memory()
+    for r, c in enumerate(cases):
+        host[r] = torch.cat(parts(c))
+    stage = torch.zeros(blob, dtype=torch.uint8, device="cuda")
+    o = [0]
+    for n in sizes:
+        o.append(o[-1] + n)
+    c0 = cases[0]
+    views = (stage[o[0]:o[1]].view(torch.bfloat16).view(c0.kv.shape),
+             stage[o[1]:o[2]].view(torch.bfloat16).view(c0.cos.shape),
+             stage[o[2]:o[3]].view(torch.bfloat16).view(c0.sin.shape), stage[o[3]:o[4]].view(torch.int64))
+    ckv = sentinel_cache((512, 128, 1, 512), "bf16")
+    k = sentinel_cache((512, 128, 1, 64), "bf16")
+    call = kvr.prepare_kv_rmsnorm_rope_cache(views[0], c0.gamma.cuda(), views[1], views[2], views[3], ckv, k,
+                                             cache_mode="PA_BSND")
+    for r in range(len(cases)):
+        call.staged(host[r], stage, blob)
+    torch.cuda.synchronize()
+    r_ckv = r_k = None
+    for c in cases:
+        c.gamma = c0.gamma
+        r_ckv, r_k, _ = run_oracle_kv(c, r_ckv, r_k) if r_ckv is not None else run_oracle_kv(c)
+    compare_cache(codes_of(ckv), r_ckv, "bf16", 512)
+    compare_cache(codes_of(k), r_k, "bf16", 64)
+
+
 def test_benchmark_decode_sets_match_the_oracle():
     """The rotating decode batches the benchmark times, through the same
     call and launch configuration, against the oracle (first four sets)."""
