@@ -139,6 +139,19 @@ def test_kv_staged_host_validation(lib, kw, call, want):
                                             c["host_status"], None) == want
 
 
+def test_debug_validation_switch_keeps_host_validation_first(lib):
+    """With the debug index check on, host validation still decides first
+    (no index copy is attempted for an invalid call), and an empty problem is
+    still OK without touching the device; the switch can be turned off again."""
+    lib.kvr_set_debug_validate(1)
+    try:
+        assert lib.kv_rmsnorm_rope_cache(ctypes.byref(_kv_args(kv=None)), None) == N.KVR_ERR_NULL
+        assert lib.kv_rmsnorm_rope_cache(ctypes.byref(_kv_args(Dk=63)), None) == N.KVR_ERR_SHAPE
+        assert lib.kv_rmsnorm_rope_cache(ctypes.byref(_kv_args(Bkv=0, kv=None, index=None)), None) == N.KVR_OK
+    finally:
+        lib.kvr_set_debug_validate(0)
+
+
 def test_kv_empty_problem_is_ok_without_launch(lib):
     a = _kv_args(Bkv=0, kv=None, index=None)
     assert lib.kv_rmsnorm_rope_cache(ctypes.byref(a), None) == N.KVR_OK
