@@ -81,3 +81,17 @@ def test_cpu_baseline_on_several_processes():
     tps, procs, batches, secs = res
     assert procs == 2 and batches >= 2 and secs >= 0.5
     assert 0.1 * one[0] < tps / procs < 10 * one[0]
+
+
+def test_algorithmic_bytes_of_the_workloads():
+    """The bytes each workload must move, worked out by hand from its sizes:
+    decode 251 active rows x (1152 kv + 256 cos/sin + 8 index + 1024 + 128
+    cache) + 5 skipped index entries + 1 KB gamma; prefill 32768 rows; the FP8
+    workload with 512-byte ckv rows and a 2 KB scale; QSA 1024 blocks of 64
+    rows x 256 B + first-token cos/sin 256 B + key 256 B, 32 key_length
+    entries, 256 B weight; DynamicQuant 32768 rows of 1024 + 512 + 4 B."""
+    assert bench.kv_algorithmic_bytes(251, 5) == 251 * 2568 + 5 * 8 + 1024 == 645632
+    assert bench.kv_algorithmic_bytes(32768, 0) == 84149248
+    assert bench.kv_algorithmic_bytes(4096, 0, ckv_bytes=1, scale_bytes=2048) == 4096 * 2056 + 1024 + 2048
+    assert bench.qsa_algorithmic_bytes(1024, 32, 64, 128, 64) == 1024 * (16384 + 256 + 256) + 256 + 256 == 17302016
+    assert bench.dq_algorithmic_bytes(32768, 512) == 32768 * 1540 == 50462720
