@@ -3,6 +3,7 @@
 // are invalid; see include/kvr.h for the contract.
 #include <atomic>
 #include <cstdlib>
+#include <initializer_list>
 #include <mutex>
 #include <unordered_set>
 #include <vector>
@@ -90,6 +91,19 @@ bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
 }
 
 kvr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVR_OK : KVR_ERR_CUDA; }
+
+// True when every factor is nonnegative and their product stays below 2^62,
+// so that the element offsets and byte counts derived from it cannot
+// overflow int64.
+bool product_fits(std::initializer_list<int64_t> factors) {
+    int64_t p = 1;
+    for (int64_t x : factors) {
+        if (x < 0) return false;
+        if (x != 0 && p > (int64_t(1) << 62) / x) return false;
+        p *= x;
+    }
+    return true;
+}
 
 // Debug validation: -1 until the environment (KVR_DEBUG_VALIDATE=1) has
 // been read, then 0 or 1; kvr_set_debug_validate() overrides it.
@@ -196,6 +210,9 @@ kvr_status kv_plan(const kvr_kv_args* a, KvPlan* plan, bool* empty) {
     const int64_t D = a->Dv + a->Dk;
     const int64_t stride = a->kv_row_stride == 0 ? D : a->kv_row_stride;
     if (stride < D) return KVR_ERR_SHAPE;
+    if (!product_fits({a->Bkv, a->Skv, stride, 2}) || !product_fits({a->Bkv, a->Skv, a->Dk, 4}) ||
+        !product_fits({a->cache_d0, a->cache_d1, D, 2}))
+        return KVR_ERR_SHAPE;
     if (a->mode == KVR_CACHE_NORM && a->cache_d0 < a->Bkv) return KVR_ERR_SHAPE;
     if (!(a->eps >= 0.f) || !(a->kc_scale == a->kc_scale)) return KVR_ERR_SHAPE;
     const int64_t T = a->Bkv * a->Skv;
@@ -388,6 +405,10 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
         return KVR_ERR_SHAPE;
     if (rope && (a->Dr < 2 || (a->Dr & 1) || a->Dr > a->Di)) return KVR_ERR_SHAPE;
     if (!(a->eps >= 0.f)) return KVR_ERR_SHAPE;
+    if (!product_fits({a->N, a->L, a->Di, 2}) || !product_fits({a->N, a->Bcap, a->Di, 2}) ||
+        !product_fits({a->N, a->Bp, a->Di, 2}) || !product_fits({a->N, a->key_block_size, a->Di, 2}) ||
+        !product_fits({a->key_length_len, 8}))
+        return KVR_ERR_SHAPE;
     // Concat-output form: the past block keys come from a separate buffer.
     const bool concat = a->past_block_index_keys != nullptr && a->past_block_index_keys != a->block_keys;
     // Without new tokens only the carry outputs and the past-row copy remain.
@@ -487,7 +508,8 @@ kvr_status dynamic_quant(const kvr_dq_args* a, cudaStream_t stream) {
     if (a == nullptr) return KVR_ERR_NULL;
     if (!is16(a->in_dtype)) return KVR_ERR_DTYPE;
     const int64_t stride = a->q_row_stride == 0 ? a->Hckv : a->q_row_stride;
-    if (a->rows < 0 || a->Hckv < 1 || stride < a->Hckv) return KVR_ERR_SHAPE;
+    if (a->rows < 0 || a->Hckv < 1 || stride < a->Hckv || !product_fits({a->rows, stride, 2}))
+        return KVR_ERR_SHAPE;
     if (a->rows == 0) return KVR_OK;
     if (a->q_nope == nullptr || a->q_out == nullptr || a->dequant_scale == nullptr) return KVR_ERR_NULL;
     if (!aligned(a->q_nope, 2) || !aligned(a->dequant_scale, 4)) return KVR_ERR_SHAPE;

@@ -115,6 +115,8 @@ def _kv_args(**kw):
     (dict(index=(1 << 20) * 5 + 4), N.KVR_ERR_SHAPE),                         # misaligned int64
     (dict(ckv_cache=(1 << 20) + 64), N.KVR_ERR_ALIAS),                        # cache over kv
     (dict(k_cache=(1 << 20) * 64 + 1024), N.KVR_ERR_ALIAS),                   # caches overlap
+    (dict(Bkv=1 << 31, Skv=1 << 31), N.KVR_ERR_SHAPE),                        # kv offsets would overflow
+    (dict(cache_d0=1 << 40, cache_d1=1 << 20), N.KVR_ERR_SHAPE),              # cache offsets would overflow
 ])
 def test_kv_host_validation(lib, kw, want):
     a = _kv_args(**kw)
@@ -191,6 +193,8 @@ def _qsa_args(**kw):
     (dict(rope_layout=4), N.KVR_ERR_MODE),
     (dict(rope_layout=-1), N.KVR_ERR_MODE),
     (dict(Bp=-1), N.KVR_ERR_SHAPE),
+    (dict(N=1 << 31, L=1 << 30), N.KVR_ERR_SHAPE),                 # key offsets would overflow
+    (dict(Bcap=1 << 60), N.KVR_ERR_SHAPE),
     (dict(past_block_index_keys=(1 << 20) * 8 + 256, Bp=4), N.KVR_ERR_ALIAS),     # overlaps block_keys
     (dict(past_block_index_keys=(1 << 20) * 64, Bp=4,
           next_incomplete_raw_keys=(1 << 20) * 64 + 32), N.KVR_ERR_ALIAS),       # carry out over it
@@ -215,6 +219,7 @@ def test_qsa_empty_problem_is_ok(lib):
     (dict(in_dtype=N.KVR_INT8), N.KVR_ERR_DTYPE),
     (dict(Hckv=0), N.KVR_ERR_SHAPE),
     (dict(rows=-1), N.KVR_ERR_SHAPE),
+    (dict(rows=1 << 60), N.KVR_ERR_SHAPE),                        # row offsets would overflow
     (dict(q_row_stride=100), N.KVR_ERR_SHAPE),
     (dict(q_nope=None), N.KVR_ERR_NULL),
     (dict(dequant_scale=None), N.KVR_ERR_NULL),
