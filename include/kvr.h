@@ -35,7 +35,8 @@
  *     the host-staged entry point copies back, asynchronously, and the index
  *     that the opt-in debug validation, kvr_set_debug_validate, checks).
  *   - Host-side errors (a NULL that is required, a bad shape, dtype or
- *     mode) are returned before any launch; nothing is written.
+ *     mode) are returned before any launch; nothing is written. Sizes whose
+ *     element offsets or byte counts would reach 2^62 are KVR_ERR_SHAPE.
  *   - Data-dependent errors are found on the device: the offending row or
  *     block is skipped (never written out of bounds) and, if `dev_status`
  *     is non-NULL, the matching KVR_DEVERR_* bit is OR-ed into *dev_status.
