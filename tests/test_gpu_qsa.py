@@ -107,11 +107,13 @@ def test_pipeline_ring_depths(N, L, Di, Dr, kbs):
     assert n == case.completed_blocks()
 
 
-# ---- RoPE layouts on each kernel variant: bulk copies (Di, Dr multiples of
-# 8), register loads (Dr not a multiple of 8), scalar loads (Di odd multiple of 4) ----
+# ---- RoPE layouts on each kernel variant: one warp per block (Di, kbs
+# compiled: 128, 64), bulk copies (Di, Dr multiples of 8, other kbs: 128, 64,
+# 5 and 16, 16, 2), register loads (Dr not a multiple of 8), scalar loads (Di
+# odd multiple of 4) ----
 
 @pytest.mark.parametrize("layout", ["interleave_last", "interleave_first", "half_last", "half_first"])
-@pytest.mark.parametrize("Di,Dr,kbs", [(128, 64, 64), (24, 6, 5), (12, 4, 3), (16, 16, 2)])
+@pytest.mark.parametrize("Di,Dr,kbs", [(128, 64, 64), (128, 64, 5), (24, 6, 5), (12, 4, 3), (16, 16, 2)])
 def test_rope_layouts(layout, Di, Dr, kbs):
     case = wl.make_qsa_case("l", 5, 37, Di=Di, Dr=Dr, kbs=kbs, seed=Di * 3 + kbs, past_max=300)
     n, _ = check(case, rope_layout=layout)
