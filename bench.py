@@ -57,8 +57,8 @@ def parse_args(argv=None):
                     help="CPU work budget of the oracle baseline leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--extras-only", action="store_true", help="time only the other workloads")
-    ap.add_argument("--only", choices=["prefill_paged", "quant_fp8", "tiny_norm", "qsa_prepare", "decode_paged",
-                                       "dynamic_quant_decode"],
+    ap.add_argument("--only", choices=["prefill_paged", "quant_fp8", "tiny_norm", "qsa_prepare",
+                                       "qsa_prepare_params_ready", "decode_paged", "dynamic_quant_decode"],
                     help="run W + K launches of one workload and print their timing (for profilers)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
@@ -778,13 +778,14 @@ def run_only(args):
     from attention_prologue_kv_gb300.build import build
     build()
     dev = torch.device("cuda", 0)
-    if args.only == "qsa_prepare":
+    if args.only in ("qsa_prepare", "qsa_prepare_params_ready"):
         q = wl.qsa_prepare_workload()
         bk = torch.zeros(q.N, q.Bcap, q.Di, dtype=torch.bfloat16, device=dev)
         d = lambda t: t.to(dev)
         a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
              d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
-        fn = lambda: kvr.qsa_prepare(*a)
+        pr = args.only == "qsa_prepare_params_ready"
+        fn = lambda: kvr.qsa_prepare(*a, params_ready=pr)
     elif args.only == "dynamic_quant_decode":
         q = wl.dynamic_quant_decode().to(dev)
         o = torch.empty(q.shape, dtype=torch.int8, device=dev)
