@@ -67,7 +67,8 @@ class DqArgs(ctypes.Structure):
     ]
 
 
-EXPORTS = ("kv_rmsnorm_rope_cache", "kv_rmsnorm_rope_cache_staged", "qsa_prepare", "dynamic_quant", "kvr_device_copy",
+EXPORTS = ("kv_rmsnorm_rope_cache", "kv_rmsnorm_rope_cache_staged", "kv_rmsnorm_rope_cache_staged_static",
+           "qsa_prepare", "dynamic_quant", "kvr_device_copy",
            "kvr_check_bounded_wait", "kvr_set_debug_validate",
            "kvr_status_string", "kvr_abi_version")
 
@@ -90,6 +91,9 @@ def lib():
     L.kv_rmsnorm_rope_cache.restype = _int
     L.kv_rmsnorm_rope_cache_staged.argtypes = [ctypes.POINTER(KvArgs), _vp, _vp, _i64, _vp, _vp]
     L.kv_rmsnorm_rope_cache_staged.restype = _int
+    L.kv_rmsnorm_rope_cache_staged_static.argtypes = [ctypes.POINTER(KvArgs), _vp, _i64, _i64, _i64, _i64, _i64,
+                                                      _vp, _vp]
+    L.kv_rmsnorm_rope_cache_staged_static.restype = _int
     L.qsa_prepare.argtypes = [ctypes.POINTER(QsaArgs), _vp]
     L.qsa_prepare.restype = _int
     L.dynamic_quant.argtypes = [ctypes.POINTER(DqArgs), _vp]

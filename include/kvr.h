@@ -203,6 +203,49 @@ kvr_status kv_rmsnorm_rope_cache(const kvr_kv_args* args, cudaStream_t stream);
 kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* args, const void* host_src, void* dev_dst, int64_t bytes,
                                         int32_t* host_status, cudaStream_t stream);
 
+/* Largest packed input, in bytes, that kv_rmsnorm_rope_cache_staged_static
+ * stages: 8 MiB (a 256-token decode batch of the 512 + 64 split packs into
+ * 354 KiB, a 4096-token batch into 5.5 MiB). */
+#define KVR_STATIC_STAGE_BYTES (8 * 1024 * 1024)
+
+/*
+ * kv_rmsnorm_rope_cache_staged for callers that cannot allocate device memory
+ * (no counterpart on the pages). The host-staged call needs a device buffer
+ * to copy the step's inputs into, and some callers have none to give: code
+ * running where cudaMalloc is not allowed (inside an allocator's own
+ * callbacks, or under a framework that owns all device memory and offers its
+ * plugins no way to ask for more) or a process whose memory budget is spent.
+ * This entry point allocates nothing: it stages into one area of
+ * KVR_STATIC_STAGE_BYTES that the library holds as a static device array on
+ * every device that loads it, from load until the process exits.
+ *
+ *   args        as for kv_rmsnorm_rope_cache, except that args->kv, cos, sin
+ *               and index are ignored: those four inputs are read from the
+ *               staging area at the byte offsets below.
+ *   host_src    `bytes` bytes of packed inputs in host memory (pinned for the
+ *               copy to run as a kernel, as for kv_rmsnorm_rope_cache_staged);
+ *               kv at kv_offset, cos at cos_offset, sin at sin_offset (each a
+ *               multiple of 2) and index at index_offset (a multiple of 8),
+ *               laid out as kv_rmsnorm_rope_cache expects them.
+ *   bytes       at most KVR_STATIC_STAGE_BYTES; every input must lie inside
+ *               [0, bytes), so each byte the call reads was written by its own
+ *               copy and nothing in the area has to start at zero.
+ *   host_status as for kv_rmsnorm_rope_cache_staged.
+ *
+ * Errors: bytes < 0 or > KVR_STATIC_STAGE_BYTES, or an input outside
+ * [0, bytes) or misaligned: KVR_ERR_SHAPE, nothing enqueued; everything else
+ * as kv_rmsnorm_rope_cache_staged (KVR_ERR_CUDA if the area's address cannot
+ * be found). The first call on each device looks up the area's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture on the device. All calls on a device
+ * share the one area, which keeps the last call's contents: calls on the same
+ * stream are ordered, but calls that can run at the same time on the GPU
+ * (other streams, other host threads) overwrite each other's inputs.
+ */
+kvr_status kv_rmsnorm_rope_cache_staged_static(const kvr_kv_args* args, const void* host_src, int64_t bytes,
+                                               int64_t kv_offset, int64_t cos_offset, int64_t sin_offset,
+                                               int64_t index_offset, int32_t* host_status, cudaStream_t stream);
+
 /* Which Dr channels the QSA rotation acts on and how it pairs them (the
  * qsa_prepare page names neither). Every layout writes pair i's results to
  * lanes i and i + Dr/2 of the rotated channels with cos/sin lanes i and
