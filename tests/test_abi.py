@@ -255,3 +255,22 @@ def test_bounded_wait_check_validation(lib):
     assert lib.kvr_check_bounded_wait(1 << 20, 10, 0, None) == N.KVR_ERR_SHAPE            # limit below 1 us
     assert lib.kvr_check_bounded_wait(1 << 20, 2 * 10**9, 0, None) == N.KVR_ERR_SHAPE      # above 1 s
     assert lib.kvr_check_bounded_wait(1 << 20, 100000, 200000, None) == N.KVR_ERR_SHAPE    # abort after the limit
+
+
+def test_static_staging_host_validation(lib):
+    """The no-allocation staged call refuses, before any device work, a
+    request larger than its static area (8 MiB) or inputs outside the copied
+    bytes; an empty problem is OK and copies nothing."""
+    big = 8 * 1024 * 1024
+    call = lambda a, nbytes, offs: lib.kv_rmsnorm_rope_cache_staged_static(
+        ctypes.byref(a), 1 << 41, nbytes, offs[0], offs[1], offs[2], offs[3], None, None)
+    a = _kv_args(kv=None, cos=None, sin=None, index=None)          # the four inputs come from the area
+    T = 2 * 3
+    offs = [0, T * 576 * 2, T * 576 * 2 + T * 128, T * 576 * 2 + T * 256]
+    total = offs[3] + T * 8
+    assert call(a, big + 16, offs) == N.KVR_ERR_SHAPE
+    assert call(a, -1, offs) == N.KVR_ERR_SHAPE
+    assert call(a, total - 8, offs) == N.KVR_ERR_SHAPE                        # index past the copied bytes
+    assert call(a, total, [0, offs[1] + 1, offs[2], offs[3]]) == N.KVR_ERR_SHAPE   # misaligned cos
+    assert call(a, total, [0, offs[1], offs[2], offs[3] + 4]) == N.KVR_ERR_SHAPE   # misaligned index
+    assert call(_kv_args(Bkv=0, kv=None, cos=None, sin=None, index=None), total, offs) == N.KVR_OK
