@@ -20,10 +20,12 @@ ops-transformer):
   ("Formula", key path: c^KV = alpha_kv * RmsNorm(...)) multiplies the
   normalised part before it is encoded.
 
-Readings where the pages are silent: no intermediate rounding (one rounding
-to the cache type at the end); eps is a float32 value, used widened; an
-8-bit code is decided from the float32 value of y*scale (the precision the
-GPU path takes that decision in), 16-bit outputs round once from float64.
+Readings where the pages are silent: everything is float64 with no
+intermediate rounding, and each output takes one rounding to its cache type
+at the end: 16-bit outputs round y (or r) once, 8-bit codes are decided
+from the float64 product y * scale and rounded once. eps and alpha_kv are
+taken as the values the caller passes (the C call receives them as float32;
+the tests hand the oracle those same values).
 """
 import math
 
@@ -63,16 +65,15 @@ def quantise(y, dtype, scale):
     """Encode one result vector for a cache of element type `dtype`.
 
     16-bit caches take one RNE rounding from float64 and no scale. 8-bit
-    caches take encode(y * scale) where the product is first rounded to
-    float32, the precision in which the GPU path decides the code."""
+    caches take encode(y * scale): the float64 product, rounded once to the
+    code."""
     if dtype in enc.DTYPES_16:
         if scale is not None:
             raise ValueError("a 16-bit cache takes no quantisation scale")
         return enc.encode(y, dtype)
     if scale is None:
         raise ValueError("an 8-bit cache needs a quantisation scale")
-    v = (y * np.asarray(scale, dtype=np.float64)).astype(np.float32).astype(np.float64)
-    return enc.encode(v, dtype)
+    return enc.encode(y * np.asarray(scale, dtype=np.float64), dtype)
 
 
 def cache_slot(mode, b, s, index, Skv, d0, d1):
@@ -127,8 +128,8 @@ def ref_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache, *,
     ckv_cache / k_cache: code arrays (uint16 or uint8) [d0, d1, Dv] / [d0, d1, Dk]
     """
     Bkv, Skv, D = kv.shape
-    eps = float(np.float32(eps))
-    alpha = float(np.float32(kc_scale))
+    eps = float(eps)
+    alpha = float(kc_scale)
     d0, d1 = ckv_cache.shape[0], ckv_cache.shape[1]
     y = alpha * rms_norm(kv[..., :Dv], gamma, eps)           # [Bkv, Skv, Dv]
     r = interleave_rope(kv[..., Dv:], cos, sin)              # [Bkv, Skv, Dk]
@@ -157,8 +158,8 @@ def ref_kv_rmsnorm_rope_cache_loop(kv, gamma, cos, sin, index, ckv_cache, k_cach
     Bkv, Skv, D = kv.shape
     Dk = D - Dv
     h = Dk // 2
-    eps = float(np.float32(eps))
-    alpha = float(np.float32(kc_scale))
+    eps = float(eps)
+    alpha = float(kc_scale)
     d0, d1 = ckv_cache.shape[0], ckv_cache.shape[1]
     status = 0
     for b in range(Bkv):

@@ -93,7 +93,7 @@ def ref_qsa_prepare(raw, block_keys, key_length, rope_cos, rope_sin, k_norm_weig
     N, L, Di = raw.shape
     kbs = int(key_block_size)
     Bcap = block_keys.shape[1]
-    eps = float(np.float32(eps))
+    eps = float(eps)
     Dr = 0 if rope_cos is None else rope_cos.shape[-1]
     status = 0
     for n in range(N):

@@ -24,6 +24,12 @@ def evs(exprs):
     return np.array([ev(e) for e in exprs], dtype=np.float64)
 
 
+def f32_arg(x):
+    """The value a float argument of the C call holds (it is passed as a
+    C float): what the oracle must be given for the same call."""
+    return float(np.float32(x))
+
+
 def f64(t):
     """torch tensor (bf16/f16/f32) -> float64 numpy array (exact widening)."""
     if t is None:
@@ -62,11 +68,11 @@ def run_oracle_kv(case, ckv=None, k=None, loop=False):
         ckv, k = sentinel_caches_np(case)
     kv, gamma, cos, sin, index = oracle_kv_inputs(case)
     fn = oracle.ref_kv_rmsnorm_rope_cache_loop if loop else oracle.ref_kv_rmsnorm_rope_cache
-    st = fn(kv, gamma, cos, sin, index, ckv, k, Dv=case.Dv, mode=case.mode, eps=case.eps,
+    st = fn(kv, gamma, cos, sin, index, ckv, k, Dv=case.Dv, mode=case.mode, eps=f32_arg(case.eps),
             ckv_dtype=case.ckv_dtype, k_dtype=case.k_dtype,
             ckv_scale=None if case.ckv_scale is None else case.ckv_scale.numpy(),
             k_scale=None if case.k_scale is None else case.k_scale.numpy(),
-            kc_scale=case.kc_scale)
+            kc_scale=f32_arg(case.kc_scale))
     return ckv, k, st
 
 
@@ -74,7 +80,7 @@ def oracle_qsa_inputs(case):
     return dict(raw=f64(case.raw), key_length=case.key_length.numpy(),
                 rope_cos=f64(case.rope_cos), rope_sin=f64(case.rope_sin),
                 k_norm_weight=f64(case.k_norm_weight), past_raw=f64(case.past_raw),
-                past_rope=f64(case.past_rope), key_block_size=case.kbs, eps=case.eps)
+                past_rope=f64(case.past_rope), key_block_size=case.kbs, eps=f32_arg(case.eps))
 
 
 def run_oracle_qsa(case, block_keys=None, carry=False, rope_layout="interleave_last",
@@ -222,3 +228,30 @@ def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="int
     for c in checks:
         c()
     return codes_of(bk), f64(nr), f64(npr), int(status.item())
+
+
+DQ_NEAR_TIE = 2.0 ** -14   # DynamicQuant quotients this close to a half-integer may round either way
+
+
+def compare_dynamic_quant(g_codes, g_scale, q64, exact=False):
+    """DynamicQuant GPU results against the float64 oracle on rows q64.
+
+    Scales: RowMax/127 rounded once to float32 on both sides, so equal.
+    Codes: within one code of round-half-even(q*127/RowMax); equal wherever
+    that quotient is at least DQ_NEAR_TIE from a half-integer (the kernel's
+    reciprocal product is within 2^-15.4 of it); with exact, equal
+    everywhere. Returns the fraction of equal codes."""
+    from oracle.dynamic_quant import dynamic_quant_quotients, ref_dynamic_quant
+    codes, s = ref_dynamic_quant(q64)
+    v, _ = dynamic_quant_quotients(q64)
+    g = np.asarray(g_codes).reshape(codes.shape)
+    assert np.array_equal(np.asarray(g_scale).reshape(-1), s), "scales differ"
+    d = np.abs(g.astype(np.int64) - codes.astype(np.int64))
+    assert d.max(initial=0) <= 1, "codes differ by %d" % int(d.max())
+    if exact:
+        assert d.max(initial=0) == 0, "%d codes differ in exact mode" % int((d > 0).sum())
+    else:
+        far = np.abs(np.abs(v - np.rint(v)) - 0.5) >= DQ_NEAR_TIE
+        assert np.array_equal(g[far], codes[far]), "%d codes away from a tie differ" % int(
+            (g[far] != codes[far]).sum())
+    return float(np.mean(d == 0)) if d.size else 1.0

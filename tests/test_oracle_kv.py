@@ -36,6 +36,25 @@ def test_quant_toy_codes():
         assert list(got.astype(int)) == [w if w >= 0 else w + 256 for w in want], dt
 
 
+def test_quantise_rounds_the_float64_product_once():
+    """An 8-bit code is one rounding of the float64 product y * scale: values
+    just past a rounding midpoint by less than float32 can resolve still round
+    away from the midpoint (a float32 intermediate would land on the midpoint
+    and tie to even instead)."""
+    eps = 2.0 ** -40
+    one = np.array([1.0])
+    # int8: 2.5 + eps -> 3 (via float32: 2.5 -> 2)
+    assert oracle.quantise(np.array([2.5 + eps]), "int8", one)[0] == 3
+    assert oracle.quantise(np.array([-2.5 - eps]), "int8", one)[0] == np.uint8(256 - 3)
+    # E4M3FN: midpoint of 1.0 (0x38) and 1.125 (0x39) is 1.0625
+    assert oracle.quantise(np.array([1.0625 + eps]), "fp8_e4m3fn", one)[0] == 0x39
+    assert oracle.quantise(np.array([1.0625]), "fp8_e4m3fn", one)[0] == 0x38
+    # E5M2: midpoint of 1.0 (0x3C) and 1.25 (0x3D) is 1.125
+    assert oracle.quantise(np.array([1.125 + eps]), "fp8_e5m2", one)[0] == 0x3D
+    # the product itself is not rounded first: y = 1 + 2**-30, scale = 2.5 -> 2.5 + 2.5 * 2**-30 -> 3
+    assert oracle.quantise(np.array([1.0 + 2.0 ** -30]), "int8", np.array([2.5]))[0] == 3
+
+
 def test_rope_identity_angle_is_deinterleave():
     rng = np.random.default_rng(1)
     x = rng.standard_normal((5, 64))
