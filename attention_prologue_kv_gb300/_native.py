@@ -5,7 +5,7 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvr.so")
-ABI_VERSION = 7   # KVR_ABI_VERSION of include/kvr.h these structures mirror
+ABI_VERSION = 8   # KVR_ABI_VERSION of include/kvr.h these structures mirror
 
 # kvr_status
 KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS, KVR_ERR_CUDA, KVR_ERR_INDEX = range(8)
@@ -63,7 +63,7 @@ class DqArgs(ctypes.Structure):
     _fields_ = [
         ("q_nope", _vp), ("in_dtype", _int),
         ("rows", _i64), ("Hckv", _i64), ("q_row_stride", _i64),
-        ("q_out", _vp), ("dequant_scale", _vp),
+        ("q_out", _vp), ("dequant_scale", _vp), ("exact", ctypes.c_int32),
     ]
 
 

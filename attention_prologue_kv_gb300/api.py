@@ -340,12 +340,13 @@ def check_bounded_wait(dev_status, limit_us, abort_after_us=0, stream=None):
         raise KvrError(st, "kvr_check_bounded_wait")
 
 
-def dynamic_quant(q_nope, q_out, dequant_scale, *, stream=None):
+def dynamic_quant(q_nope, q_out, dequant_scale, *, exact=False, stream=None):
     """DynamicQuant of q^N: per row (last axis, e.g. q^N [T, N, Hckv] gives
     T*N rows) dequant_scale = RowMax(|q|)/127 and q_out = round(q/scale) as
     int8. q_nope bf16/f16 with a dense last axis and uniformly strided rows;
     q_out int8 of q_nope's shape (dense); dequant_scale float32 with one
-    element per row (e.g. [T, N, 1])."""
+    element per row (e.g. [T, N, 1]). Codes are within one code of
+    round(q*127/RowMax); exact=True makes every code equal to it."""
     _cuda(q_nope, "q_nope")
     if q_nope.dtype not in _IN_DTYPES:
         raise ValueError("q_nope must be bfloat16 or float16")
@@ -364,7 +365,7 @@ def dynamic_quant(q_nope, q_out, dequant_scale, *, stream=None):
         raise ValueError("dequant_scale must be float32 with one element per row")
     a = N.DqArgs(q_nope=q2.data_ptr(), in_dtype=_IN_DTYPES[q_nope.dtype], rows=rows, Hckv=H,
                  q_row_stride=stride, q_out=_ptr(q_out, "q_out"),
-                 dequant_scale=_ptr(dequant_scale, "dequant_scale"))
+                 dequant_scale=_ptr(dequant_scale, "dequant_scale"), exact=1 if exact else 0)
     st = N.lib().dynamic_quant(ctypes.byref(a), _stream(stream))
     if st != N.KVR_OK:
         raise KvrError(st, "dynamic_quant")

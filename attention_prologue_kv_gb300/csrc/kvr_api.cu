@@ -525,6 +525,7 @@ kvr_status dynamic_quant(const kvr_dq_args* a, cudaStream_t stream) {
     p.rows = a->rows;
     p.H = a->Hckv;
     p.q_stride = stride;
+    p.exact = a->exact != 0;
     const bool vec = a->Hckv % 8 == 0 && a->Hckv <= 1024 && stride % 8 == 0 && aligned(a->q_nope, 16) &&
                      aligned(a->q_out, 8);
     (void)cudaGetLastError();

@@ -283,6 +283,7 @@ struct DqParams {
     int8_t* out;
     float* scale;
     int64_t rows, H, q_stride;
+    int exact;           // recompute near-tie codes from the exact rational
 };
 
 // Launch with programmatic stream serialisation allowed: the grid may be

@@ -13,13 +13,14 @@
 // routine that allocates device memory.
 //
 // Host code cannot use the array's name as a device address (in host code
-// the name denotes a host-side stand-in), so the first call on each device
-// looks the address up with cudaGetSymbolAddress while that device is
-// current, checks the result, and keeps it for later calls on that device.
-// Device code could name the array directly; the kernels here receive the
-// looked-up address as an ordinary pointer.
-#include <mutex>
-
+// the name denotes a host-side stand-in), so every call looks the address up
+// with cudaGetSymbolAddress in the current context and checks the result.
+// The lookup allocates nothing; it is redone on every call rather than kept,
+// because a kept address goes stale when the device is reset or when the
+// caller runs in a context other than the one it was looked up in. The first
+// lookup on a device may load this library's device code there. Device code
+// could name the array directly; the kernels here receive the looked-up
+// address as an ordinary pointer.
 #include "kvr_internal.cuh"
 
 // The staging area (KVR_STATIC_STAGE_BYTES, declared in kvr.h).
@@ -27,27 +28,14 @@ static __device__ __align__(256) unsigned char kvr_static_stage[KVR_STATIC_STAGE
 
 namespace {
 
-std::mutex g_stage_mu;
-void* g_stage_addr[64] = {};   // per device ordinal: device address of kvr_static_stage
-
-// Device address of the staging area on the current device, looked up once
-// per device.
+// Device address of the staging area in the current context.
 kvr_status static_stage_address(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, kvr_static_stage) != cudaSuccess || p == nullptr) {
         (void)cudaGetLastError();
         return KVR_ERR_CUDA;
     }
-    std::lock_guard<std::mutex> lock(g_stage_mu);
-    if (g_stage_addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, kvr_static_stage) != cudaSuccess || p == nullptr) {
-            (void)cudaGetLastError();
-            return KVR_ERR_CUDA;
-        }
-        g_stage_addr[dev] = p;
-    }
-    *out = g_stage_addr[dev];
+    *out = p;
     return KVR_OK;
 }
 

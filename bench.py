@@ -1,16 +1,18 @@
 #!/usr/bin/env python3
 """Benchmark of the fused KV prologue (RMSNorm + interleaved RoPE + paged
-cache scatter) on the decode workload, plus the other workloads as extras.
+cache scatter) on the prefill workload, plus the other workloads as extras.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = one kv_rmsnorm_rope_cache call on one decode batch: Bkv = 256
-tokens, Skv = 1, D = 512 + 64 bf16, PA_BSND cache BlockSize 128 x BlockNum
-4096, 5 of 256 index entries -1. Steps rotate over 512 independent input
-sets (185 MB > L2), so every step reads its inputs from HBM. The K timed
-steps run as CUDA-graph replays of back-to-back calls (a graph of one
-512-step rotation, replayed, plus a remainder graph), timed with CUDA events
-on the capture stream. With N > 1 (torchrun) each rank runs an independent
+One step = one kv_rmsnorm_rope_cache call on one prefill batch: Bkv = 8
+sequences x Skv = 4096 tokens (32768 token rows), D = 512 + 64 bf16, kv
+~N(0, std 2), positions 0..4095, PA_BSND caches BlockSize 128 x BlockNum
+2048 written through a random per-sequence block table. Steps rotate over 4
+independent input sets (186 MB > L2), so every step reads its inputs from
+HBM. The K timed steps run as CUDA-graph replays of back-to-back calls (a
+graph of one rotation, replayed, plus a remainder graph; each graph is
+replayed once, untimed, before the timed region), timed with CUDA events on
+the capture stream. With N > 1 (torchrun) each rank runs an independent
 replica on its own GPU; the job value sums tokens over ranks and divides by
 the slowest rank's time (weak scaling, no data-path collective).
 
@@ -18,7 +20,8 @@ Printed on rank 0: one JSON line with the metric, the roofline of the kernel,
 the CPU oracle baseline (one process, and one spawned process per host core
 under "all_cores"), the end-to-end figure (host buffers, host<->device
 copies inside the timed region), clocks sampled during the timed region, and
-the other workloads (prefill, FP8 quantised, QSA prepare) under "extras".
+the other workloads (decode, FP8 quantised, QSA prepare, DynamicQuant) under
+"extras" as microseconds per call and fractions of the measured HBM peak.
 """
 import argparse
 import datetime
@@ -36,15 +39,15 @@ if ROOT not in sys.path:
 
 METRIC = "tokens/s and achieved HBM GB/s (% of GB300 peak) for fused norm+RoPE+cache write"
 UNIT = "tokens/s"
-ROTATION = 512           # input sets rotated through by the decode steps
-DEFAULT_STEPS = 102400   # 200 rotations, ~0.3 s of GPU time
-DEFAULT_WARMUP = 1024
-WORKLOAD = ("decode_paged: Bkv=256 Skv=1 N=1 D=576 (Dv=512 rmsnorm, Dk=64 interleaved RoPE) bf16, "
-            "kv ~N(0,1), gamma ~U(0.5,1.5), positions ~U[0,32768), PA_BSND bf16 caches "
-            "BlockSize=128 BlockNum=4096, 256 distinct slots per batch with 5 (2%) set to -1")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kv_rmsnorm_rope_cache__decode_paged.md")
+ROTATION = 4             # input sets rotated through by the prefill steps
+DEFAULT_STEPS = 2048     # 512 rotations, ~30 ms of GPU time
+DEFAULT_WARMUP = 16
+WORKLOAD = ("prefill_paged: Bkv=8 Skv=4096 (32768 tokens) N=1 D=576 (Dv=512 rmsnorm, Dk=64 interleaved RoPE) "
+            "bf16, kv ~N(0,std 2), gamma ~U(0.5,1.5), positions 0..4095, PA_BSND bf16 caches BlockSize=128 "
+            "BlockNum=2048, slots from a random per-sequence block table")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kv_bulk_kernel__prefill_paged.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "attention_prologue_kv_gb300", "csrc", f)
-                  for f in ("kv_rmsnorm_rope_cache.cu", "kv_common.cuh", "kvr_internal.cuh")]
+                  for f in ("kv_bulk.cu", "kv_common.cuh", "kvr_internal.cuh")]
 
 
 def parse_args(argv=None):
@@ -58,7 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--extras-only", action="store_true", help="time only the other workloads")
     ap.add_argument("--only", choices=["prefill_paged", "quant_fp8", "tiny_norm", "qsa_prepare",
-                                       "qsa_prepare_params_ready", "decode_paged", "dynamic_quant_decode"],
+                                       "qsa_prepare_params_ready", "decode_paged", "dynamic_quant_decode",
+                                       "dynamic_quant_decode_exact"],
                     help="run W + K launches of one workload and print their timing (for profilers)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
@@ -266,40 +270,46 @@ def time_each(fn, n, flush, stream):
     return statistics.median(ts), min(ts)
 
 
-def _oracle_inputs(sets, n):
-    """The first n decode batches as the oracle's float64 / int64 arrays."""
-    kv = sets["kv"][:n].double().numpy().reshape(n, -1, 1, 576)
-    cos = sets["cos"][:n].double().numpy().reshape(n, -1, 1, 64)
-    sin = sets["sin"][:n].double().numpy().reshape(n, -1, 1, 64)
-    return kv, cos, sin, sets["index"][:n].numpy(), sets["gamma"].double().numpy()
+def _oracle_seqs(case, n):
+    """The first n sequences of a PA_BSND KV case as the oracle's float64 /
+    int64 arrays, one tuple (kv [1, Skv, D], cos, sin [1, Skv, Dk], index [Skv])
+    per sequence, and gamma."""
+    D, Dk = case.Dv + case.Dk, case.Dk
+    kv = case.kv.double().reshape(case.Bkv, case.Skv, D).numpy()
+    cos = case.cos.double().reshape(case.Bkv, case.Skv, Dk).numpy()
+    sin = case.sin.double().reshape(case.Bkv, case.Skv, Dk).numpy()
+    idx = case.index.numpy().reshape(case.Bkv, case.Skv)
+    seqs = [(kv[b:b + 1], cos[b:b + 1], sin[b:b + 1], idx[b]) for b in range(min(n, case.Bkv))]
+    return seqs, case.gamma.double().numpy()
 
 
-def _oracle_loop(budget_s, kv, cos, sin, index, gamma, d0, d1):
-    """The oracle as it stands on decode batches (cycled) for about budget_s
-    seconds: (tokens/s, batches, seconds)."""
+def _oracle_loop(budget_s, seqs, gamma, d0, d1, Dv):
+    """The oracle as it stands on whole sequences (cycled) for about budget_s
+    seconds: (tokens/s, sequences, seconds)."""
     import numpy as np
 
     import oracle
-    ckv = np.full((d0, d1, 512), 0x7FBF, dtype=np.uint16)
-    kc = np.full((d0, d1, 64), 0x7FBF, dtype=np.uint16)
-    n_tok, n_batch = 0, 0
+    Dk = seqs[0][1].shape[-1]
+    ckv = np.full((d0, d1, Dv), 0x7FBF, dtype=np.uint16)
+    kc = np.full((d0, d1, Dk), 0x7FBF, dtype=np.uint16)
+    n_tok, n_seq = 0, 0
     t0 = time.perf_counter()
     while True:
-        i = n_batch % kv.shape[0]
-        oracle.ref_kv_rmsnorm_rope_cache(kv[i], gamma, cos[i], sin[i], index[i], ckv, kc,
-                                         Dv=512, mode="PA_BSND", eps=1e-6)
+        kv, cos, sin, idx = seqs[n_seq % len(seqs)]
+        oracle.ref_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, idx, ckv, kc, Dv=Dv, mode="PA_BSND", eps=1e-6)
         n_tok += kv.shape[1]
-        n_batch += 1
+        n_seq += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return n_tok / el, n_batch, el
+    return n_tok / el, n_seq, el
 
 
-def cpu_oracle_baseline(budget_s, sets, d0, d1):
-    """The oracle as it stands, on decode batches of the same workload, for
-    about budget_s seconds of single-process CPU time. Returns tokens/s."""
-    return _oracle_loop(budget_s, *_oracle_inputs(sets, min(16, sets["kv"].shape[0])), d0, d1)
+def cpu_oracle_baseline(budget_s, case):
+    """The oracle as it stands, on whole sequences of the workload, for about
+    budget_s seconds of single-process CPU time: (tokens/s, sequences, s)."""
+    seqs, gamma = _oracle_seqs(case, 2)
+    return _oracle_loop(budget_s, seqs, gamma, case.d0, case.d1, case.Dv)
 
 
 def _oracle_process(budget_s, inputs, barrier, out):
@@ -309,20 +319,21 @@ def _oracle_process(budget_s, inputs, barrier, out):
     out.put(_oracle_loop(budget_s, *inputs))
 
 
-def cpu_oracle_all_cores(budget_s, sets, d0, d1, n=None):
+def cpu_oracle_all_cores(budget_s, case, n=None):
     """The same oracle in one process per host core (n processes if given;
-    spawned, so no process inherits a CUDA context; each gets its own decode
-    batches), started together: aggregate tokens/s."""
+    spawned, so no process inherits a CUDA context; each gets one sequence of
+    the workload and its own caches), started together: aggregate
+    (tokens/s, processes, sequences, seconds)."""
     import multiprocessing as mp
     n = n or os.cpu_count() or 1
     ctx = mp.get_context("spawn")
     barrier, out = ctx.Barrier(n), ctx.Queue()
-    kv, cos, sin, index, gamma = _oracle_inputs(sets, min(16, sets["kv"].shape[0]))
+    seqs, gamma = _oracle_seqs(case, case.Bkv)
     procs = []
     for i in range(n):
-        j = [i % kv.shape[0]]
         procs.append(ctx.Process(target=_oracle_process,
-                                 args=(budget_s, (kv[j], cos[j], sin[j], index[j], gamma, d0, d1), barrier, out)))
+                                 args=(budget_s, ([seqs[i % len(seqs)]], gamma, case.d0, case.d1, case.Dv),
+                                       barrier, out)))
     for p in procs:
         p.start()
     res, deadline = [], time.time() + 600
@@ -341,12 +352,18 @@ def cpu_oracle_all_cores(budget_s, sets, d0, d1, n=None):
     return sum(r[0] for r in res), n, sum(r[1] for r in res), max(r[2] for r in res)
 
 
+def prefill_sets(n, rank=0):
+    """n independent prefill batches (CPU tensors); the benchmark uses the
+    first one's gamma for all of them (one model weight)."""
+    from attention_prologue_kv_gb300 import workloads as wl
+    return [wl.prefill_paged(seed=1003 + 7919 * i + 100003 * rank) for i in range(n)]
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     import attention_prologue_kv_gb300 as kvr
-    from attention_prologue_kv_gb300 import workloads as wl
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -358,49 +375,46 @@ def run_ours(args):
         build()
     barrier()
 
-    # ---- inputs: ROTATION decode batches resident in HBM ----
-    sets = wl.decode_paged_sets(ROTATION, seed=1002 + 100003 * rank)
+    # ---- inputs: ROTATION prefill batches resident in HBM ----
     R = ROTATION
-    kv = sets["kv"].to(dev)
-    cos = sets["cos"].to(dev)
-    sin = sets["sin"].to(dev)
-    index = sets["index"].to(dev)
-    gamma = sets["gamma"].to(dev)
-    d0, d1 = sets["d0"], sets["d1"]
-    ckv = torch.full((d0, d1, 1, 512), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
-    kc = torch.full((d0, d1, 1, 64), wl.SENTINEL16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    cases = prefill_sets(R, rank)
+    c0 = cases[0]
+    kv = [c.kv.to(dev) for c in cases]
+    cos = [c.cos.to(dev) for c in cases]
+    sin = [c.sin.to(dev) for c in cases]
+    index = [c.index.to(dev) for c in cases]
+    gamma = c0.gamma.to(dev)
+    d0, d1 = c0.d0, c0.d1
+    ckv = torch.full((d0, d1, 1, c0.Dv), 0x7FBF, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    kc = torch.full((d0, d1, 1, c0.Dk), 0x7FBF, dtype=torch.int16, device=dev).view(torch.bfloat16)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    n_skip = (sets["index"] == -1).sum(dim=1)
-    Bkv = kv.shape[1]
+    T = c0.T
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
-
-    def step(i):
-        kvr.kv_rmsnorm_rope_cache(kv[i], gamma, cos[i], sin[i], index[i], ckv, kc,
-                                  cache_mode="PA_BSND", eps=1e-6, dev_status=status)
+    calls = [kvr.prepare_kv_rmsnorm_rope_cache(kv[i], gamma, cos[i], sin[i], index[i], ckv, kc,
+                                               cache_mode="PA_BSND", eps=1e-6, dev_status=status)
+             for i in range(R)]
 
     # ---- warm-up: W eager steps ----
     for w in range(args.warmup):
-        step((R - 1 - w) % R)
+        calls[w % R]()
     torch.cuda.synchronize()
 
-    # ---- graphs: one full rotation, plus the remainder ----
+    # ---- graphs: one full rotation, plus the remainder; each replayed once untimed ----
     K = args.steps
     full, rem = divmod(K, R)
-    g_full = g_rem = None
-    if full:
-        g_full = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_full):
-            for i in range(R):
-                step(i)
-    if rem:
-        g_rem = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_rem):
-            for i in range(rem):
-                step(i)
-    if g_full is not None:
-        g_full.replay()      # one untimed replay: graph upload and first-launch costs
+    graphs = []
+    for n in ([R] if full else []) + ([rem] if rem else []):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                calls[i]()
+        graphs.append(g)
+    for g in graphs:
+        g.replay()           # graph upload and first-launch costs stay out of the timed region
     torch.cuda.synchronize()
+    g_full = graphs[0] if full else None
+    g_rem = graphs[-1] if rem else None
     stream = torch.cuda.current_stream()
 
     sampler = ClockSampler(gpu_smi_id(local)) if rank == 0 else None
@@ -425,16 +439,12 @@ def run_ours(args):
     clocks = sampler.stop(wall0, wall1) if sampler else None
     assert int(status.item()) == 0, "device status %d" % int(status.item())
 
-    tokens = Bkv * K
+    tokens = T * K
     job_ms, job_tokens = reduce_timing(elapsed_ms, tokens, dev)
     value = job_tokens / (job_ms / 1e3)
-
-    # per-launch algorithmic bytes, averaged over the sets the K steps used
-    used = [i % R for i in range(K)] if K < R else list(range(R))
-    skips = [int(n_skip[i]) for i in used]
-    avg_bytes = statistics.fmean(kv_algorithmic_bytes(Bkv - s, s) for s in skips)
+    nbytes = kv_algorithmic_bytes(T, 0, c0.Dv, c0.Dk)
     per_launch_s = elapsed_ms / 1e3 / K
-    achieved = avg_bytes / per_launch_s / 1e9
+    achieved = nbytes / per_launch_s / 1e9
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
@@ -442,35 +452,38 @@ def run_ours(args):
 
     result = None
     if rank == 0:
-        # ---- end to end: host buffers, one packed H2D copy per step, status read back ----
-        e2e = e2e_decode(args, sets, gamma, ckv, kc, dev, kvr)
-        extras = None if args.no_extras else run_extras(dev, kvr, wl, flush_buf)
-        cpu_tps, n_batches, cpu_s = cpu_oracle_baseline(args.cpu_seconds, sets, d0, d1)
-        all_cores = cpu_oracle_all_cores(max(1.0, args.cpu_seconds / 2), sets, d0, d1)
+        e2e = e2e_prefill(args, cases, gamma, ckv, kc, dev, kvr)
+        del kv, cos, sin, index, calls, graphs, g_full, g_rem
+        torch.cuda.empty_cache()
+        extras = None if args.no_extras else run_extras(dev, kvr, flush_buf, peak)
+        cpu_tps, n_seq, cpu_s = cpu_oracle_baseline(args.cpu_seconds, c0)
+        all_cores = cpu_oracle_all_cores(max(1.0, args.cpu_seconds / 2), c0)
+        in_mb = R * T * ((c0.Dv + c0.Dk) * 2 + 4 * c0.Dk + 8) / 1e6
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": job_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD,
-                       "step": "one kv_rmsnorm_rope_cache call on one 256-token decode batch",
+                       "step": "one kv_rmsnorm_rope_cache call on one 32768-token prefill batch",
                        "l2": "inputs larger than L2: steps rotate over %d input sets (%.0f MB > %.0f MB L2)"
-                             % (R, (kv.numel() + cos.numel() * 2) * 2 / 1e6 + index.numel() * 8 / 1e6, l2 / 1e6),
-                       "launch": "CUDA graph replays of back-to-back calls (%d x %d-step graph + %d-step graph)"
-                                 % (full, R, rem),
+                             % (R, in_mb, l2 / 1e6),
+                       "launch": "CUDA graph replays of back-to-back calls (%d x %d-step graph + %d-step "
+                                 "graph, each replayed once untimed first)" % (full, R, rem),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src,
-                         "bytes_per_launch": avg_bytes, "launch_us": per_launch_s * 1e6,
+                         "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                         else peak_src,
+                         "kernel": "kv_bulk_kernel", "bytes_per_launch": nbytes, "launch_us": per_launch_s * 1e6,
                          "traffic_source": PROFILE_SUMMARY.replace(ROOT + "/", "") if traffic else traffic_state},
             "cpu_baseline": {"value": cpu_tps, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "%d decode batches of 256 tokens (%.1f s, float64 NumPy, one process)"
-                                       % (n_batches, cpu_s),
+                             "sample": "%d whole 4096-token sequences of the prefill batch (%.1f s, float64 "
+                                       "NumPy, one process)" % (n_seq, cpu_s),
                              "all_cores": None if all_cores is None else {
                                  "value": all_cores[0], "unit": UNIT, "cores": all_cores[1],
-                                 "sample": "%d processes (one per host core, spawned, started together), "
-                                           "%d decode batches of 256 tokens in %.1f s" % all_cores[1:]}},
+                                 "sample": "%d spawned processes, one per host core, %d sequences in %.1f s"
+                                           % all_cores[1:]}},
             "e2e": e2e,
             "gpu_launches": K,
             "clocks": clocks,
@@ -481,26 +494,27 @@ def run_ours(args):
     return result
 
 
-def e2e_decode(args, sets, gamma, ckv, kc, dev, kvr):
+def e2e_prefill(args, cases, gamma, ckv, kc, dev, kvr):
     """Same metric through the public API with the inputs in pinned host
     memory: per step one host->device copy of the packed batch, the call, and
     a device->host read of the status word; timed over the K steps."""
     import torch
-    R = sets["kv"].shape[0]
-    kvb = sets["kv"][0].numel() * 2
-    csb = sets["cos"][0].numel() * 2
-    ixb = sets["index"][0].numel() * 8
+    R = len(cases)
+    c0 = cases[0]
+    kvb = c0.kv.numel() * 2
+    csb = c0.cos.numel() * 2
+    ixb = c0.index.numel() * 8
     blob = kvb + 2 * csb + ixb
     host = torch.empty(R, blob, dtype=torch.uint8).pin_memory()
-    host[:, :kvb] = sets["kv"].reshape(R, -1).view(torch.uint8)
-    host[:, kvb:kvb + csb] = sets["cos"].reshape(R, -1).view(torch.uint8)
-    host[:, kvb + csb:kvb + 2 * csb] = sets["sin"].reshape(R, -1).view(torch.uint8)
-    host[:, kvb + 2 * csb:] = sets["index"].reshape(R, -1).view(torch.uint8)
+    for i, c in enumerate(cases):
+        host[i, :kvb] = c.kv.reshape(-1).view(torch.uint8)
+        host[i, kvb:kvb + csb] = c.cos.reshape(-1).view(torch.uint8)
+        host[i, kvb + csb:kvb + 2 * csb] = c.sin.reshape(-1).view(torch.uint8)
+        host[i, kvb + 2 * csb:] = c.index.reshape(-1).view(torch.uint8)
     stage = torch.empty(blob, dtype=torch.uint8, device=dev)
-    B = sets["kv"].shape[1]
-    kv_v = stage[:kvb].view(torch.bfloat16).view(B, 1, 1, -1)
-    cos_v = stage[kvb:kvb + csb].view(torch.bfloat16).view(B, 1, 1, -1)
-    sin_v = stage[kvb + csb:kvb + 2 * csb].view(torch.bfloat16).view(B, 1, 1, -1)
+    kv_v = stage[:kvb].view(torch.bfloat16).view(c0.kv.shape)
+    cos_v = stage[kvb:kvb + csb].view(torch.bfloat16).view(c0.cos.shape)
+    sin_v = stage[kvb + csb:kvb + 2 * csb].view(torch.bfloat16).view(c0.sin.shape)
     idx_v = stage[kvb + 2 * csb:].view(torch.int64)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     K = args.steps
@@ -519,7 +533,7 @@ def e2e_decode(args, sets, gamma, ckv, kc, dev, kvr):
     def one(i, k):
         staged(host_ptr[i], stage_ptr, blob, st_ptr + 4 * k, sid)
 
-    for w in range(min(args.warmup, 64)):
+    for w in range(max(args.warmup, 3)):
         one(w % R, 0)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -533,16 +547,16 @@ def e2e_decode(args, sets, gamma, ckv, kc, dev, kvr):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     assert int(st_host.max()) == 0
-    return {"value": B * K / wall, "unit": UNIT, "h2d_bytes_per_step": blob, "d2h_bytes_per_step": 4,
+    return {"value": c0.T * K / wall, "unit": UNIT, "h2d_bytes_per_step": blob, "d2h_bytes_per_step": 4,
             "device_ms": e0.elapsed_time(e1), "wall_ms": wall * 1e3,
-            "how": "public API: prepare_kv_rmsnorm_rope_cache(...).staged() = the C entry point "
-                   "kv_rmsnorm_rope_cache_staged, enqueuing per step one packed pinned H2D copy, the call "
-                   "and a status D2H copy on one stream; synchronised once after the K steps"}
+            "how": "kv_rmsnorm_rope_cache_staged per step: packed pinned H2D copy, the call, status D2H; "
+                   "one stream, synchronised after the K steps"}
 
 
 def time_graph(calls, n_calls, stream):
     """Average duration of one call when n_calls calls (cycling through
-    `calls`) run back to back as one CUDA graph replay."""
+    `calls`) run back to back as one CUDA graph replay (after one untimed
+    replay)."""
     import torch
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -559,44 +573,52 @@ def time_graph(calls, n_calls, stream):
     return e0.elapsed_time(e1) / n_calls
 
 
-def run_extras(dev, kvr, wl, flush_buf):
-    """The other workloads. Each is timed two ways: isolated (one launch after
-    an L2 flush, event-timed, launch latency included) and steady (back-to-back
-    launches in a CUDA graph over input sets that together exceed L2)."""
+def run_extras(dev, kvr, flush_buf, peak):
+    """The other workloads, each as {"us": microseconds per call, "frac":
+    algorithmic bytes / time / measured HBM peak}: back-to-back calls in a
+    CUDA graph over input sets that together exceed L2."""
     import torch
+
+    from attention_prologue_kv_gb300 import workloads as wl
     out = {}
     stream = torch.cuda.current_stream()
     flush = lambda: l2_flush(flush_buf)
-    peaks = measured_peaks()
-    peak = peaks.get("hbm_gbs", 6800.0)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
-    # in-process copy reference (16-byte vectorised device copy, 2 x 512 MB)
+    def rec(us, nbytes):
+        return {"us": round(us, 3), "frac": round(nbytes / (us / 1e6) / 1e9 / peak, 4)}
+
+    # in-process copy references (16-byte vectorised device copy): 2 x 512 MB, and
+    # the prefill's size (42 MB read + 42 MB written) back to back over rotating sources
     src = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     dst = torch.empty_like(src)
-    med, best = time_each(lambda: kvr.device_copy(dst, src), 10, flush, stream)
-    copy_gbs = 2 * src.numel() / (best / 1e3) / 1e9
-    out["copy_peak_gbs_in_run"] = copy_gbs
+    _, best = time_each(lambda: kvr.device_copy(dst, src), 10, flush, stream)
+    out["copy_1GB"] = rec(best * 1e3, 2 * src.numel())
     del src, dst
-    # the same copy at the prefill's size (42 MB read + 42 MB written per call),
-    # back to back over rotating sources: what a plain copy reaches at this size
     half = 84149248 // 2 // 16 * 16
     n_pairs = int(2 * l2 // (2 * half)) + 2
     bufs = [(torch.empty(half, dtype=torch.uint8, device=dev), torch.empty(half, dtype=torch.uint8, device=dev))
             for _ in range(n_pairs)]
     calls = [lambda b=b: kvr.device_copy(b[1], b[0]) for b in bufs]
-    us = time_graph(calls, 8 * len(calls), stream) * 1e3
-    out["copy_84MB_steady"] = {"us": us, "gbs": 2 * half / (us / 1e6) / 1e9,
-                               "how": "%d (src, dst) pairs of %.0f MB rotated" % (n_pairs, half / 1e6)}
-    del bufs
+    out["copy_84MB"] = rec(time_graph(calls, 8 * len(calls), stream) * 1e3, 2 * half)
+    del bufs, calls
 
-    def summary(us_iso, us_steady, nbytes, units, unit_name):
-        gbs = nbytes / (us_steady / 1e6) / 1e9
-        return {unit_name: units, "bytes": nbytes, "us_isolated": us_iso, "us_steady": us_steady,
-                unit_name + "_per_s": units / (us_steady / 1e6), "gbs": gbs,
-                "frac_of_measured_peak": gbs / peak, "frac_of_copy_in_run": gbs / copy_gbs,
-                "frac_of_nominal_8000": gbs / 8000.0,
-                "gbs_isolated": nbytes / (us_iso / 1e6) / 1e9}
+    def nsets(bytes_per_set):
+        return max(3, int(2 * l2 // bytes_per_set) + 1)
+
+    # decode: 256-token batches, 512 sets rotated (186 MB)
+    sets = wl.decode_paged_sets(512, seed=1002)
+    d0, d1 = sets["d0"], sets["d1"]
+    ckv = torch.zeros(d0, d1, 1, 512, dtype=torch.bfloat16, device=dev)
+    kc = torch.zeros(d0, d1, 1, 64, dtype=torch.bfloat16, device=dev)
+    kv, cs, sn, ix = (sets[k].to(dev) for k in ("kv", "cos", "sin", "index"))
+    gamma = sets["gamma"].to(dev)
+    calls = [kvr.prepare_kv_rmsnorm_rope_cache(kv[i], gamma, cs[i], sn[i], ix[i], ckv, kc, cache_mode="PA_BSND")
+             for i in range(512)]
+    skips = (sets["index"] == -1).sum(dim=1).tolist()
+    nbytes = statistics.fmean(kv_algorithmic_bytes(256 - s, s) for s in skips)
+    out["decode_paged"] = rec(time_graph(calls, 4096, stream) * 1e3, nbytes)
+    del calls, kv, cs, sn, ix, ckv, kc, sets
 
     def kv_workload(make, seeds, params_ready=False):
         cases = [make(seed=s) for s in seeds]
@@ -607,82 +629,44 @@ def run_extras(dev, kvr, wl, flush_buf):
             wl.TORCH_DTYPES[c0.k_dtype])
         calls = []
         for c in cases:
-            a = (c.kv.to(dev), c.gamma.to(dev), c.cos.to(dev), c.sin.to(dev), c.index.to(dev), ckv, kc)
-            kw = dict(cache_mode=c.mode, eps=c.eps, ckv_scale=None if c.ckv_scale is None else c.ckv_scale.to(dev),
-                      params_ready=params_ready)
-            calls.append(lambda a=a, kw=kw: kvr.kv_rmsnorm_rope_cache(*a, **kw))
-        for f in calls:
-            f()
-        iso, _ = time_each(calls[0], 20, flush, stream)
-        steady = time_graph(calls, max(8 * len(calls), 48), stream)
+            calls.append(kvr.prepare_kv_rmsnorm_rope_cache(
+                c.kv.to(dev), c.gamma.to(dev), c.cos.to(dev), c.sin.to(dev), c.index.to(dev), ckv, kc,
+                cache_mode=c.mode, eps=c.eps, ckv_scale=None if c.ckv_scale is None else c.ckv_scale.to(dev),
+                params_ready=params_ready))
         act = c0.active_tokens()
         nbytes = kv_algorithmic_bytes(act, c0.T - act, c0.Dv, c0.Dk,
                                       ckv_bytes=1 if c0.ckv_dtype != "bf16" else 2,
                                       scale_bytes=0 if c0.ckv_scale is None else 4 * c0.ckv_scale.numel())
-        in_set = c0.T * ((c0.Dv + c0.Dk) * 2 + 4 * c0.Dk + 8)
-        r = summary(iso * 1e3, steady * 1e3, nbytes, c0.T, "tokens")
-        r["sets"] = "%d input sets x %.1f MB" % (len(cases), in_set / 1e6)
-        return r
+        return rec(time_graph(calls, max(8 * len(calls), 48), stream) * 1e3, nbytes)
 
-    def nsets(bytes_per_set):
-        return max(3, int(2 * l2 // bytes_per_set) + 1)
-
-    out["prefill_paged"] = kv_workload(wl.prefill_paged, [1003 + 7919 * i for i in range(3)])
     out["quant_fp8"] = kv_workload(wl.quant_fp8, [1004 + 7919 * i for i in range(nsets(4096 * 1416))])
     # the same with params_ready: gamma and the scales read before the dependency wait
     out["quant_fp8_params_ready"] = kv_workload(wl.quant_fp8, [1004 + 7919 * i for i in range(nsets(4096 * 1416))],
                                                 params_ready=True)
     out["tiny_norm"] = kv_workload(wl.tiny_norm, [1001])
 
+    # QSA prepare: default form, rotate-half on the first Dr channels, params_ready,
+    # and the concat-output form (past block keys [N, Bp, Di] copied into a fresh output first)
     qs = [wl.qsa_prepare_workload(seed=1005 + 7919 * i) for i in range(nsets(17.3e6))]
     q0 = qs[0]
+    nb = q0.completed_blocks()
+    qbytes = qsa_algorithmic_bytes(nb, q0.N, q0.kbs, q0.Di, q0.Dr)
     bk = torch.zeros(q0.N, q0.Bcap, q0.Di, dtype=torch.bfloat16, device=dev)
     d = lambda t: t.to(dev)
-    calls = []
-    for q in qs:
-        a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
-             d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
-        calls.append(lambda a=a: kvr.qsa_prepare(*a))
-    for f in calls:
-        f()
-    iso, _ = time_each(calls[0], 20, flush, stream)
-    steady = time_graph(calls, 8 * len(calls), stream)
-    nb = q0.completed_blocks()
-    r = summary(iso * 1e3, steady * 1e3, qsa_algorithmic_bytes(nb, q0.N, q0.kbs, q0.Di, q0.Dr),
-                q0.N * q0.L, "new_tokens")
-    r["blocks"] = nb
-    r["sets"] = "%d input sets" % len(qs)
-    out["qsa_prepare"] = r
-
-    # the same sets with the other RoPE layout family, with params_ready (the
-    # kernel before does not write key_length, the tables or the weight), and
-    # in the concat-output form (past block keys [N, Bp, Di] copied into a
-    # fresh output first)
     Bp = int(max(max(p_ // q.kbs for p_ in q.meta["past"]) for q in qs))
     past_bk = torch.zeros(q0.N, Bp, q0.Di, dtype=torch.bfloat16, device=dev)
+    qsa_args = [(d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
+                d(q.past_raw), d(q.past_rope), q.kbs, q.eps) for q in qs]
     for name, kw, extra in (
+            ("qsa_prepare", {}, lambda q: 0),
             ("qsa_prepare_half_first", dict(rope_layout="half_first"), lambda q: 0),
             ("qsa_prepare_params_ready", dict(params_ready=True), lambda q: 0),
             ("qsa_prepare_concat", dict(past_block_index_keys=past_bk),
              lambda q: 2 * q.Di * 2 * sum(min(Bp, p_ // q.kbs) for p_ in q.meta["past"]))):
-        calls = []
-        for q in qs:
-            a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
-                 d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
-            calls.append(lambda a=a, kw=kw: kvr.qsa_prepare(*a, **kw))
-        for f in calls:
-            f()
-        iso, _ = time_each(calls[0], 20, flush, stream)
-        steady = time_graph(calls, 8 * len(calls), stream)
+        calls = [lambda a=a, kw=kw: kvr.qsa_prepare(*a, **kw) for a in qsa_args]
         extra_mean = sum(extra(q) for q in qs) / len(qs)   # copied rows differ between sets
-        nbytes = qsa_algorithmic_bytes(nb, q0.N, q0.kbs, q0.Di, q0.Dr) + extra_mean
-        r = summary(iso * 1e3, steady * 1e3, nbytes, q0.N * q0.L, "new_tokens")
-        r["blocks"] = nb
-        r["sets"] = "%d input sets" % len(qs)
-        if name == "qsa_prepare_concat":
-            r["past_rows_copied_mean"] = extra_mean / (2 * q0.Di * 2)
-        out[name] = r
-    del past_bk
+        out[name] = rec(time_graph(calls, 8 * len(calls), stream) * 1e3, qbytes + extra_mean)
+    del past_bk, qsa_args, calls, qs, bk
 
     # the same kernel at 8x the new tokens (32 x 16384): separates its fixed
     # per-call latency from its streaming rate
@@ -694,30 +678,18 @@ def run_extras(dev, kvr, wl, flush_buf):
         a = (d(q.raw), bkb, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
              d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
         calls.append(lambda a=a: kvr.qsa_prepare(*a))
-    for f in calls:
-        f()
-    iso, _ = time_each(calls[0], 10, flush, stream)
-    steady = time_graph(calls, 8 * len(calls), stream)
-    nbl = qb[0].completed_blocks()
-    r = summary(iso * 1e3, steady * 1e3, qsa_algorithmic_bytes(nbl, 32, 64, 128, 64), 32 * 16384, "new_tokens")
-    r["blocks"] = nbl
-    r["sets"] = "%d input sets" % len(qb)
-    out["qsa_prepare_L16384"] = r
+    out["qsa_prepare_L16384"] = rec(time_graph(calls, 8 * len(calls), stream) * 1e3,
+                                    qsa_algorithmic_bytes(qb[0].completed_blocks(), 32, 64, 128, 64))
     del qb, calls, bkb
 
-    # DynamicQuant of q^N for one decode step (256 tokens x 128 heads x 512)
+    # DynamicQuant of q^N for one decode step (256 tokens x 128 heads x 512), default and exact
     qs = [wl.dynamic_quant_decode(seed=1006 + 7919 * i) for i in range(nsets(256 * 128 * 512 * 2))]
     rows, H = qs[0].numel() // qs[0].shape[-1], qs[0].shape[-1]
     outs = [(q.to(dev), torch.empty(q.shape, dtype=torch.int8, device=dev),
              torch.empty(q.shape[:-1] + (1,), dtype=torch.float32, device=dev)) for q in qs]
-    calls = [lambda o=o: kvr.dynamic_quant(*o) for o in outs]
-    for f in calls:
-        f()
-    iso, _ = time_each(calls[0], 20, flush, stream)
-    steady = time_graph(calls, 8 * len(calls), stream)
-    r = summary(iso * 1e3, steady * 1e3, dq_algorithmic_bytes(rows, H), rows, "rows")
-    r["sets"] = "%d input sets" % len(qs)
-    out["dynamic_quant_decode"] = r
+    for name, exact in (("dynamic_quant_decode", False), ("dynamic_quant_decode_exact", True)):
+        calls = [lambda o=o, e=exact: kvr.dynamic_quant(*o, exact=e) for o in outs]
+        out[name] = rec(time_graph(calls, 8 * len(calls), stream) * 1e3, dq_algorithmic_bytes(rows, H))
     torch.cuda.synchronize()
     return out
 
@@ -727,43 +699,43 @@ def run_extras(dev, kvr, wl, flush_buf):
 # ---------------------------------------------------------------------------
 
 def run_reference(args):
+    """The oracle as it stands on the prefill workload: each step runs it over
+    a bounded sample of one prefill batch (whole sequences; all 8 when the
+    W + K steps fit in about two minutes)."""
+    cases = prefill_sets(2)
+    c0 = cases[0]
+    seqs = [_oracle_seqs(c, c.Bkv) for c in cases]
     import numpy as np
-    import torch
 
     import oracle
-    from attention_prologue_kv_gb300 import workloads as wl
-    sets = wl.decode_paged_sets(16, seed=1002)
-    d0, d1 = sets["d0"], sets["d1"]
-    ckv = np.full((d0, d1, 512), 0x7FBF, dtype=np.uint16)
-    kc = np.full((d0, d1, 64), 0x7FBF, dtype=np.uint16)
-    gamma = sets["gamma"].to(torch.float64).numpy()
-    B = sets["kv"].shape[1]
+    ckv = np.full((c0.d0, c0.d1, c0.Dv), 0x7FBF, dtype=np.uint16)
+    kc = np.full((c0.d0, c0.d1, c0.Dk), 0x7FBF, dtype=np.uint16)
 
-    def batch(i, ntok):
-        kv = sets["kv"][i].double().numpy().reshape(-1, 1, 576)[:ntok]
-        cos = sets["cos"][i].double().numpy().reshape(-1, 1, 64)[:ntok]
-        sin = sets["sin"][i].double().numpy().reshape(-1, 1, 64)[:ntok]
-        oracle.ref_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, sets["index"][i].numpy()[:ntok], ckv, kc,
-                                         Dv=512, mode="PA_BSND", eps=1e-6)
+    def step(i, n_seq):
+        ss, gamma = seqs[i % len(seqs)]
+        for kv, cos, sin, idx in ss[:n_seq]:
+            oracle.ref_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, idx, ckv, kc, Dv=c0.Dv, mode="PA_BSND", eps=1e-6)
 
     t = time.perf_counter()
-    batch(0, B)
-    t_full = time.perf_counter() - t
+    step(0, 1)
+    t_seq = time.perf_counter() - t
     budget = 120.0
-    ntok = B if (args.steps + args.warmup) * t_full <= budget else max(
-        1, int(B * budget / ((args.steps + args.warmup) * t_full)))
+    n_seq = int(max(1, min(c0.Bkv, budget / ((args.steps + args.warmup) * t_seq))))
     for w in range(args.warmup):
-        batch(w % 16, ntok)
+        step(w, n_seq)
     t0 = time.perf_counter()
     for k in range(args.steps):
-        batch(k % 16, ntok)
+        step(k, n_seq)
     el = time.perf_counter() - t0
+    ntok = n_seq * c0.Skv
     value = ntok * args.steps / el
-    sample = "%d of 256 tokens of each decode batch per step, float64 NumPy oracle, one process" % ntok
+    sample = ("%d of the 8 sequences (%d of 32768 tokens) of a prefill batch per step, float64 NumPy oracle, "
+              "one process" % (n_seq, ntok))
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "step": "oracle on a bounded sample of one decode batch"},
+            "data": "synthetic", "config": {"workload": WORKLOAD, "step": "oracle on a bounded sample of one "
+                                                                           "prefill batch"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -786,11 +758,12 @@ def run_only(args):
              d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
         pr = args.only == "qsa_prepare_params_ready"
         fn = lambda: kvr.qsa_prepare(*a, params_ready=pr)
-    elif args.only == "dynamic_quant_decode":
+    elif args.only in ("dynamic_quant_decode", "dynamic_quant_decode_exact"):
         q = wl.dynamic_quant_decode().to(dev)
         o = torch.empty(q.shape, dtype=torch.int8, device=dev)
         sc = torch.empty(q.shape[:-1] + (1,), dtype=torch.float32, device=dev)
-        fn = lambda: kvr.dynamic_quant(q, o, sc)
+        ex = args.only == "dynamic_quant_decode_exact"
+        fn = lambda: kvr.dynamic_quant(q, o, sc, exact=ex)
     else:
         case = getattr(wl, args.only)()
         ckv = torch.zeros(case.cache_shapes()[0], dtype=wl.code_torch_dtype(case.ckv_dtype), device=dev).view(
@@ -833,13 +806,13 @@ def main(argv=None):
         import torch
 
         import attention_prologue_kv_gb300 as kvr
-        from attention_prologue_kv_gb300 import workloads as wl
         from attention_prologue_kv_gb300.build import build
         build()
         dev = torch.device("cuda", 0)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
-        print(json.dumps({"extras": run_extras(dev, kvr, wl, flush_buf)}), flush=True)
+        peak = measured_peaks().get("hbm_gbs", 6800.0)
+        print(json.dumps({"extras": run_extras(dev, kvr, flush_buf, peak)}), flush=True)
         return 0
     res = run_ours(args)
     if res is not None:

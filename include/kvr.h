@@ -27,9 +27,12 @@
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller (the
- *     host-staged entry point also takes pinned host buffers); the library
- *     allocates no device memory and keeps no per-call state. Rows are dense
- *     and row-major unless a stride argument says otherwise.
+ *     host-staged entry points also take pinned host buffers); the library
+ *     allocates no device memory and keeps no per-call state, with one
+ *     exception: kv_rmsnorm_rope_cache_staged_static stages its inputs in a
+ *     static device array of the library, shared by all its calls on a
+ *     device. Rows are dense and row-major unless a stride argument says
+ *     otherwise.
  *   - Calls are asynchronous on `stream`: they validate on the host, launch,
  *     and return. Nothing is read back to the host (except the status word
  *     the host-staged entry point copies back, asynchronously, and the index
@@ -56,7 +59,9 @@
  *   - Results are deterministic: no atomics touch data.
  *   - Thread safe: entry points may be called concurrently from any host
  *     thread on any stream; overlapping writes to the same cache rows from
- *     concurrent calls are the caller's race.
+ *     concurrent calls are the caller's race. The exception is
+ *     kv_rmsnorm_rope_cache_staged_static: its calls that can run at the
+ *     same time on the GPU share its staging area and race on it.
  */
 #ifndef KVR_H
 #define KVR_H
@@ -68,7 +73,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 7
+#define KVR_ABI_VERSION 8
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -232,15 +237,21 @@ kvr_status kv_rmsnorm_rope_cache_staged(const kvr_kv_args* args, const void* hos
  *               copy and nothing in the area has to start at zero.
  *   host_status as for kv_rmsnorm_rope_cache_staged.
  *
- * Errors: bytes < 0 or > KVR_STATIC_STAGE_BYTES, or an input outside
- * [0, bytes) or misaligned: KVR_ERR_SHAPE, nothing enqueued; everything else
- * as kv_rmsnorm_rope_cache_staged (KVR_ERR_CUDA if the area's address cannot
- * be found). The first call on each device looks up the area's device address
- * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call before any stream capture on the device. All calls on a device
- * share the one area, which keeps the last call's contents: calls on the same
- * stream are ordered, but calls that can run at the same time on the GPU
- * (other streams, other host threads) overwrite each other's inputs.
+ * Errors: bytes < 0 or > KVR_STATIC_STAGE_BYTES: KVR_ERR_SHAPE; an input
+ * that does not fit inside [0, bytes) at its offset (the T kv rows at their
+ * row stride, the cos and sin tables, the index entries of the mode; so in
+ * particular a row width or row stride larger than `bytes`) or is misaligned:
+ * KVR_ERR_SHAPE; nothing is enqueued on these errors. Everything else as
+ * kv_rmsnorm_rope_cache_staged (KVR_ERR_CUDA if the area's address cannot be
+ * found). Every call with T > 0 looks up the area's device address in the
+ * current context (cudaGetSymbolAddress, which allocates nothing); the first
+ * such call on a device may load the library's device code there, so make
+ * it before any stream capture on the device. The address is never kept
+ * between calls, so a device reset or another context stays safe. All calls
+ * on a device share the one area, which keeps the last call's contents:
+ * calls on the same stream are ordered, but calls that can run at the same
+ * time on the GPU (other streams, other host threads) overwrite each other's
+ * inputs.
  */
 kvr_status kv_rmsnorm_rope_cache_staged_static(const kvr_kv_args* args, const void* host_src, int64_t bytes,
                                                int64_t kv_offset, int64_t cos_offset, int64_t sin_offset,
@@ -358,10 +369,18 @@ kvr_status qsa_prepare(const kvr_qsa_args* args, cudaStream_t stream);
  *   q_out           [rows, Hckv] int8 codes, dense.
  *   dequant_scale   [rows] float32 scales.
  *
- * Per row: scale = RowMax(|q|) / 127 and code = round-half-even(q / scale),
- * both float32 IEEE divisions, clamped to [-127, 127]; an all-zero row gets
- * scale 0 and codes 0. Inputs are finite. Limits: rows >= 0, Hckv >= 1; the
- * outputs must not overlap the input (KVR_ERR_ALIAS).
+ *   exact           0 (default) or 1, see below.
+ *
+ * Per row: dequant_scale = RowMax(|q|) / 127, rounded once to float32 (the
+ * IEEE division), and code = round-half-even(q / (RowMax/127)) =
+ * round-half-even(q * 127 / RowMax), clamped to [-127, 127]; an all-zero row
+ * gets scale 0 and codes 0. With exact = 0 each code is computed from a
+ * float32 reciprocal product and is within one code of that value (equal to
+ * it unless q * 127 / RowMax lies within 2^-15 of a half-integer). With
+ * exact = 1 those near-tie codes are recomputed from the exact rational, so
+ * every code equals it; this costs about a quarter more time on bf16 rows,
+ * where such quotients are common. Inputs are finite. Limits: rows >= 0,
+ * Hckv >= 1; the outputs must not overlap the input (KVR_ERR_ALIAS).
  */
 typedef struct kvr_dq_args {
     const void* q_nope;
@@ -370,6 +389,7 @@ typedef struct kvr_dq_args {
     int64_t q_row_stride;
     int8_t* q_out;
     float* dequant_scale;
+    int32_t exact;
 } kvr_dq_args;
 
 kvr_status dynamic_quant(const kvr_dq_args* args, cudaStream_t stream);

@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.kvr_abi_version() == N.ABI_VERSION == 7
+    assert lib.kvr_abi_version() == N.ABI_VERSION == 8
 
 
 def test_status_strings(lib):
@@ -272,5 +272,7 @@ def test_static_staging_host_validation(lib):
     assert call(a, -1, offs) == N.KVR_ERR_SHAPE
     assert call(a, total - 8, offs) == N.KVR_ERR_SHAPE                        # index past the copied bytes
     assert call(a, total, [0, offs[1] + 1, offs[2], offs[3]]) == N.KVR_ERR_SHAPE   # misaligned cos
-    assert call(a, total, [0, offs[1], offs[2], offs[3] + 4]) == N.KVR_ERR_SHAPE   # misaligned index
+    # misaligned index: 8 more bytes copied, so that the index still lies inside them
+    # and the 8-byte alignment rule alone refuses the call
+    assert call(a, total + 8, [0, offs[1], offs[2], offs[3] + 4]) == N.KVR_ERR_SHAPE
     assert call(_kv_args(Bkv=0, kv=None, cos=None, sin=None, index=None), total, offs) == N.KVR_OK

@@ -74,12 +74,12 @@ def test_cpu_baseline_on_several_processes():
     benchmark; two here): every process reports, the aggregate counts all of
     them, and each process's rate is of the order of the single-process rate."""
     from attention_prologue_kv_gb300 import workloads as wl
-    sets = wl.decode_paged_sets(2, seed=1002)
-    one = bench.cpu_oracle_baseline(0.5, sets, sets["d0"], sets["d1"])
-    res = bench.cpu_oracle_all_cores(0.5, sets, sets["d0"], sets["d1"], n=2)
+    case = wl.make_kv_case("b", 2, 256, mode="PA_BSND", d0=16, d1=128, seed=1003, slots="table", pos="seq")
+    one = bench.cpu_oracle_baseline(0.5, case)
+    res = bench.cpu_oracle_all_cores(0.5, case, n=2)
     assert res is not None
-    tps, procs, batches, secs = res
-    assert procs == 2 and batches >= 2 and secs >= 0.5
+    tps, procs, seqs, secs = res
+    assert procs == 2 and seqs >= 2 and secs >= 0.5
     assert 0.1 * one[0] < tps / procs < 10 * one[0]
 
 

@@ -4,13 +4,16 @@ the concat form, carry outputs and params_ready drawn from a fixed seed per
 case, so that combinations the targeted tests do not list are covered too.
 Same acceptance as the targeted tests: untouched bytes and copies
 bit-exact, 16-bit results within 2**-7*|ref| + 1e-6, 8-bit codes within one
-code, DynamicQuant codes and scales bit-exact, status bits equal."""
+code, DynamicQuant scales equal and codes within one code of the exact
+quotient's (equal away from ties, everywhere in exact mode), status bits
+equal."""
 import numpy as np
 import pytest
 import torch
 
 from attention_prologue_kv_gb300 import workloads as wl
-from helpers import compare_cache, run_gpu_kv, run_gpu_qsa, run_oracle_kv, run_oracle_qsa
+from helpers import (compare_cache, compare_dynamic_quant, run_gpu_kv, run_gpu_qsa, run_oracle_kv,
+                     run_oracle_qsa)
 
 pytestmark = pytest.mark.gpu
 
@@ -94,7 +97,6 @@ def test_qsa_random_configurations(i):
 @pytest.mark.parametrize("i", range(16))
 def test_dynamic_quant_random_configurations(i):
     import attention_prologue_kv_gb300 as kvr
-    from oracle.dynamic_quant import ref_dynamic_quant
     r = np.random.default_rng(9000 + i)
     H = int(r.choice([1, 3, 8, 24, 100, 256, 512, 1000, 1024, 1032, 2048]))
     q = wl.dynamic_quant_decode(seed=9100 + i, T=int(r.integers(1, 20)), heads=int(r.integers(1, 9)), Hckv=H,
@@ -102,11 +104,11 @@ def test_dynamic_quant_random_configurations(i):
     q = q * float(r.choice([1e-3, 1.0, 50.0]))
     out = torch.full(q.shape, 99, dtype=torch.int8, device="cuda")
     scale = torch.full(q.shape[:-1] + (1,), -1.0, dtype=torch.float32, device="cuda")
-    kvr.dynamic_quant(q.cuda(), out, scale)
+    exact = bool(i % 2)
+    kvr.dynamic_quant(q.cuda(), out, scale, exact=exact)
     torch.cuda.synchronize()
-    codes, s = ref_dynamic_quant(q.reshape(-1, H).to(torch.float64).numpy())
-    assert np.array_equal(out.cpu().reshape(-1, H).numpy(), codes)
-    assert np.array_equal(scale.cpu().reshape(-1).numpy(), s)
+    compare_dynamic_quant(out.cpu().numpy(), scale.cpu().numpy(), q.reshape(-1, H).to(torch.float64).numpy(),
+                          exact)
 
 
 @pytest.mark.parametrize("i", range(20))

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from attention_prologue_kv_gb300 import workloads as wl
-from helpers import compare_cache, run_gpu_kv, run_oracle_kv, sentinel_cache
+from helpers import codes_of, compare_cache, guarded_cache, run_gpu_kv, run_oracle_kv, sentinel_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -113,6 +113,39 @@ def test_index_length_is_checked_against_the_cache_mode():
     with pytest.raises(ValueError):   # the flattened (T, D) form implies one entry per token
         kvr.kv_rmsnorm_rope_cache(args[0].view(60, -1), args[1], args[2].view(60, -1), args[3].view(60, -1),
                                   case.index.cuda(), ckv, k, cache_mode="PA_BLK_BSND")
+
+
+@pytest.mark.parametrize("mode,pad", [("PA_BSND", 0), ("PA_BSND", 64), ("Norm", 0), ("Norm", 3)])
+def test_token_flattened_2d_form(mode, pad):
+    """The token-flattened shapes of the MLA page's BS fusion: kv (T, D) (dense,
+    or a column slice of wider rows), cos/sin (T, Dk), index (T). Each token
+    is one row: in PA_BSND it goes to slot index[t] (the same as in the 4-D
+    form); in Norm mode token t is batch t of the cache, row index[t]. Full
+    decode size in PA_BSND (256 tokens, 4096 x 128 slots), compared element
+    by element with the oracle."""
+    import attention_prologue_kv_gb300 as kvr
+    if mode == "PA_BSND":
+        case = wl.make_kv_case("t2", 256, 1, mode="PA_BSND", d0=4096, d1=128, seed=1302, skip=5,
+                               row_pad=pad)
+    else:
+        case = wl.make_kv_case("t2", 96, 1, mode="Norm", d0=100, d1=16, seed=1303, skip=7, row_pad=pad)
+    T, D, Dk = case.T, case.Dv + case.Dk, case.Dk
+    kv2 = case.meta["wide"].cuda()[:, :D]
+    assert kv2.dim() == 2 and kv2.shape == (T, D) and kv2.is_contiguous() == (pad == 0)
+    ckv, c1 = guarded_cache(case.cache_shapes()[0], "bf16")
+    k, c2 = guarded_cache(case.cache_shapes()[1], "bf16")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvr.kv_rmsnorm_rope_cache(kv2, case.gamma.cuda(), case.cos.reshape(T, Dk).cuda(),
+                              case.sin.reshape(T, Dk).cuda(), case.index.reshape(T).cuda(), ckv, k,
+                              cache_mode=mode, eps=case.eps, dev_status=status)
+    torch.cuda.synchronize()
+    c1()
+    c2()
+    ref_ckv, ref_k, ref_st = run_oracle_kv(case)
+    assert int(status.item()) == ref_st == 0
+    n1, _ = compare_cache(codes_of(ckv), ref_ckv, "bf16", case.Dv)
+    n2, _ = compare_cache(codes_of(k), ref_k, "bf16", case.Dk)
+    assert n1 == n2 == case.active_tokens()
 
 
 def test_misaligned_pointers_take_the_generic_path():

@@ -1,6 +1,7 @@
 """The host-staged KV call that allocates nothing
 (kv_rmsnorm_rope_cache_staged_static) against the host-staged call that
-copies into a device buffer the caller allocated (kv_rmsnorm_rope_cache_staged).
+copies into a device buffer the caller allocated (kv_rmsnorm_rope_cache_staged)
+and against the float64 oracle.
 
 Callers that cannot allocate device memory (code running inside an
 allocator's own callbacks, plugins of a framework that owns all device
@@ -8,8 +9,8 @@ memory, processes whose memory budget is spent) cannot provide that buffer;
 the new entry point stages into a static device array of the library instead.
 Both entry points are called here through the C ABI, twice in a row on two
 different batches, and after each call the caches and the status word the
-new one leaves must match the existing one's within the parity tests'
-tolerance. Requests that do not fit the array are refused before anything
+new one leaves must match the existing one's, and the oracle's, within the
+parity tests' tolerance. Requests that do not fit the array are refused before anything
 runs. This file is collected last, so a run that stops at the first failure
 has run every other test before it."""
 import ctypes
@@ -20,7 +21,7 @@ import torch
 
 from attention_prologue_kv_gb300 import _native as N
 from attention_prologue_kv_gb300 import workloads as wl
-from helpers import codes_of, compare_cache, sentinel_cache
+from helpers import codes_of, compare_cache, run_oracle_kv, sentinel_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +54,8 @@ def test_static_staging_matches_the_staged_call_twice_in_a_row():
     a = wl.make_kv_case("na", 256, 1, mode="PA_BSND", d0=64, d1=128, seed=801, skip=5)
     b = wl.make_kv_case("nb", 256, 1, mode="PA_BSND", d0=64, d1=128, seed=802, skip=3)
     b.index[17] = 64 * 128 + 5          # out of range: skipped, KVR_DEVERR_INDEX in the status word
-    gamma = a.gamma.cuda()              # one set of weights for both batches
+    b.gamma = a.gamma                   # one set of weights for both batches
+    gamma = a.gamma.cuda()
     valid = lambda c: {int(x) for x in c.index.tolist() if 0 <= x < 64 * 128}
     rows_after = [len(valid(a)), len(valid(a) | valid(b))]
     batches = [_packed(a), _packed(b)]
@@ -74,6 +76,7 @@ def test_static_staging_matches_the_staged_call_twice_in_a_row():
     args_new = _args(a, gamma, ckv, k, st)
     hs_ref = torch.full((2,), -1, dtype=torch.int32).pin_memory()
     hs = torch.full((2,), -1, dtype=torch.int32).pin_memory()
+    r_ckv = r_k = None                  # the oracle's caches, carried across the two calls
 
     for i, (host, _) in enumerate(batches):
         r = lib.kv_rmsnorm_rope_cache_staged(ctypes.byref(args_ref), host.data_ptr(), stage.data_ptr(), nbytes,
@@ -86,6 +89,11 @@ def test_static_staging_matches_the_staged_call_twice_in_a_row():
         assert int(hs[i]) == int(hs_ref[i]) == (0 if i == 0 else N.KVR_DEVERR_INDEX)
         n1, _ = compare_cache(codes_of(ckv), codes_of(ckv_ref), "bf16", 512)
         n2, _ = compare_cache(codes_of(k), codes_of(k_ref), "bf16", 64)
+        assert n1 == n2 == rows_after[i]
+        r_ckv, r_k, r_st = run_oracle_kv((a, b)[i], r_ckv, r_k)
+        assert r_st == (0 if i == 0 else N.KVR_DEVERR_INDEX)
+        n1, _ = compare_cache(codes_of(ckv), r_ckv, "bf16", 512)
+        n2, _ = compare_cache(codes_of(k), r_k, "bf16", 64)
         assert n1 == n2 == rows_after[i]
     assert int(st.item()) == int(st_ref.item()) == N.KVR_DEVERR_INDEX
 
