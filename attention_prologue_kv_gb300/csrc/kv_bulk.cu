@@ -12,6 +12,10 @@
 // here the in-flight data lives in shared memory instead:
 //  * one persistent CTA per SM; warp 0 is the producer, BULK_CONSUMERS warps
 //    compute;
+//  * CTA b owns one contiguous range of about T / gridDim rows (starting on
+//    an even row), cut into tiles of up to R rows: every SM moves the same
+//    bytes (dealing whole tiles round-robin left 7 tiles on some SMs and 6
+//    on others for a 32768-row prefill);
 //  * a tile is R consecutive token rows; per tile the producer issues one
 //    bulk copy for the kv rows (one per row when rows are strided), one for
 //    the cos rows, one for the sin rows and one for the index entries, all
@@ -67,7 +71,9 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t ntiles = (p.T + p.R - 1) / p.R;
+    // This CTA's rows [lo, hi): even starts keep the index tiles 16-byte aligned.
+    const int64_t lo = (p.T * int64_t(blockIdx.x) / gridDim.x) & ~int64_t(1);
+    const int64_t hi = blockIdx.x + 1 == gridDim.x ? p.T : ((p.T * int64_t(blockIdx.x + 1) / gridDim.x) & ~int64_t(1));
     const uint32_t kv_row = uint32_t(Dv + Dk) * 2;
     const uint32_t cs_row = uint32_t(Dk) * 2;
 
@@ -80,10 +86,8 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
         fence_mbar_init();
 #if KVR_BULK_PREFETCH
         int64_t it = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles && it < int64_t(KVR_BULK_PREFETCH) * p.S;
-             tile += gridDim.x, ++it) {
-            const int64_t r0 = tile * p.R;
-            const int rows = int(p.T - r0 < p.R ? p.T - r0 : p.R);
+        for (int64_t r0 = lo; r0 < hi && it < int64_t(KVR_BULK_PREFETCH) * p.S; r0 += p.R, ++it) {
+            const int rows = int(hi - r0 < p.R ? hi - r0 : p.R);
             if (p.kv_contig) prefetch_l2_bulk(static_cast<const char*>(p.kv) + r0 * kv_row, rows * kv_row);
             prefetch_l2_bulk(static_cast<const char*>(p.cos) + r0 * cs_row, rows * cs_row);
             prefetch_l2_bulk(static_cast<const char*>(p.sin) + r0 * cs_row, rows * cs_row);
@@ -100,14 +104,13 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
         const uint64_t policy = l2_policy_evict_first();
         int64_t it = 0;
         bool ok = true;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        for (int64_t r0 = lo; r0 < hi; r0 += p.R, ++it) {
             const int s = int(it % p.S);
             if (it >= p.S && !mbar_wait_warp(&empty[s], uint32_t(((it / p.S) - 1) & 1), abort_flag)) {
                 ok = false;
                 break;
             }
-            const int64_t r0 = tile * p.R;
-            const int rows = int(p.T - r0 < p.R ? p.T - r0 : p.R);
+            const int rows = int(hi - r0 < p.R ? hi - r0 : p.R);
             const int idx_rows = p.idx_bulk ? (rows & ~1) : 0;
             unsigned char* st = stages + size_t(s) * p.stage_bytes;
             if (lane == 0) mbar_arrive_expect_tx(&full[s], rows * kv_row + 2 * rows * cs_row + idx_rows * 8);
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
 
     const int cw = warp - 1;
     int64_t it = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    for (int64_t r0 = lo; r0 < hi; r0 += p.R, ++it) {
         const int s = int(it % p.S);
         if (!mbar_wait_warp(&full[s], uint32_t((it / p.S) & 1), abort_flag)) {
             if (lane == 0) {
@@ -160,12 +163,12 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
             }
             break;
         }
-        const int64_t r0 = tile * p.R;
-        const int rows = int(p.T - r0 < p.R ? p.T - r0 : p.R);
+        const int rows = int(hi - r0 < p.R ? hi - r0 : p.R);
         const int idx_rows = p.idx_bulk ? (rows & ~1) : 0;
         const unsigned char* st = stages + size_t(s) * p.stage_bytes;
         // Rows are dealt round-robin over the consumer warps across stages:
-        // this CTA's q-th row goes to warp q % BULK_CONSUMERS.
+        // this CTA's q-th row goes to warp q % BULK_CONSUMERS (every tile
+        // but the range's last has R rows, so q = it * R + r).
         const int first = int((cw - (it * p.R) % BULK_CONSUMERS + BULK_CONSUMERS) % BULK_CONSUMERS);
         for (int r = first; r < rows; r += BULK_CONSUMERS) {
             const int64_t t = r0 + r;
@@ -236,7 +239,7 @@ static uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 // Shared memory the ring may use per CTA (one CTA per SM), and the largest
 // tile (rows per stage).
 #ifndef KVR_BULK_RING_KB
-#define KVR_BULK_RING_KB 160
+#define KVR_BULK_RING_KB 200
 #endif
 #ifndef KVR_BULK_MAX_ROWS
 #define KVR_BULK_MAX_ROWS 32

@@ -275,6 +275,24 @@ KV_WORKLOADS = {
 }
 
 
+def prefill_paged_sets(n_sets, seed=1003):
+    """`n_sets` prefill batches shaped like prefill_paged, each from its own
+    seed, whose block tables use disjoint cache blocks (n_sets * 256 of the
+    2048 blocks, from one random permutation), so that no two batches of a
+    rotation write the same cache rows."""
+    cases = [prefill_paged(seed=seed + 7919 * i) for i in range(n_sets)]
+    c0 = cases[0]
+    nb = -(-c0.Skv // c0.d1)
+    if n_sets * c0.Bkv * nb > c0.d0:
+        raise ValueError("too many sets for disjoint block tables")
+    perm = torch.randperm(c0.d0, generator=torch.Generator().manual_seed(seed + 1))
+    s = torch.arange(c0.Skv)
+    for i, c in enumerate(cases):
+        table = perm[i * c.Bkv * nb:(i + 1) * c.Bkv * nb].view(c.Bkv, nb)
+        c.index = (table[:, s // c.d1] * c.d1 + s % c.d1).reshape(-1).contiguous().to(torch.int64)
+    return cases
+
+
 def decode_paged_sets(n_sets, seed=1002, Bkv=256, Dv=512, Dk=64, block_num=4096, block_size=128,
                       n_skip=5, pos_max=32768):
     """`n_sets` independent decode batches shaped like decode_paged, stacked:

@@ -8,11 +8,12 @@ One step = one kv_rmsnorm_rope_cache call on one prefill batch: Bkv = 8
 sequences x Skv = 4096 tokens (32768 token rows), D = 512 + 64 bf16, kv
 ~N(0, std 2), positions 0..4095, PA_BSND caches BlockSize 128 x BlockNum
 2048 written through a random per-sequence block table. Steps rotate over 4
-independent input sets (186 MB > L2), so every step reads its inputs from
-HBM. The K timed steps run as CUDA-graph replays of back-to-back calls (a
-graph of one rotation, replayed, plus a remainder graph; each graph is
-replayed once, untimed, before the timed region), timed with CUDA events on
-the capture stream. With N > 1 (torchrun) each rank runs an independent
+independent input sets (186 MB > L2) whose block tables are disjoint, so
+every step reads its inputs from HBM and writes rows no other step of the
+rotation writes. The K timed steps run as CUDA-graph replays of back-to-back
+calls (graphs of up to 256 calls cycling through the rotation, plus a
+remainder graph; each graph is replayed once, untimed, before the timed
+region), timed with CUDA events on the capture stream. With N > 1 (torchrun) each rank runs an independent
 replica on its own GPU; the job value sums tokens over ranks and divides by
 the slowest rank's time (weak scaling, no data-path collective).
 
@@ -40,11 +41,12 @@ if ROOT not in sys.path:
 METRIC = "tokens/s and achieved HBM GB/s (% of GB300 peak) for fused norm+RoPE+cache write"
 UNIT = "tokens/s"
 ROTATION = 4             # input sets rotated through by the prefill steps
+GRAPH_CALLS = 256        # calls per captured CUDA graph (cycling through the rotation)
 DEFAULT_STEPS = 2048     # 512 rotations, ~30 ms of GPU time
 DEFAULT_WARMUP = 16
 WORKLOAD = ("prefill_paged: Bkv=8 Skv=4096 (32768 tokens) N=1 D=576 (Dv=512 rmsnorm, Dk=64 interleaved RoPE) "
             "bf16, kv ~N(0,std 2), gamma ~U(0.5,1.5), positions 0..4095, PA_BSND bf16 caches BlockSize=128 "
-            "BlockNum=2048, slots from a random per-sequence block table")
+            "BlockNum=2048, slots from a random per-sequence block table (the rotated batches use disjoint blocks)")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kv_bulk_kernel__prefill_paged.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "attention_prologue_kv_gb300", "csrc", f)
                   for f in ("kv_bulk.cu", "kv_common.cuh", "kvr_internal.cuh")]
@@ -64,6 +66,9 @@ def parse_args(argv=None):
                                        "qsa_prepare_params_ready", "decode_paged", "dynamic_quant_decode",
                                        "dynamic_quant_decode_exact"],
                     help="run W + K launches of one workload and print their timing (for profilers)")
+    ap.add_argument("--profile-range", action="store_true",
+                    help="with --only: launch the K steps back to back inside one cudaProfilerStart/Stop range "
+                         "(no per-launch timing), for a profiler's range replay")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -353,10 +358,11 @@ def cpu_oracle_all_cores(budget_s, case, n=None):
 
 
 def prefill_sets(n, rank=0):
-    """n independent prefill batches (CPU tensors); the benchmark uses the
-    first one's gamma for all of them (one model weight)."""
+    """n independent prefill batches (CPU tensors) writing disjoint cache
+    blocks; the benchmark uses the first one's gamma for all of them (one
+    model weight)."""
     from attention_prologue_kv_gb300 import workloads as wl
-    return [wl.prefill_paged(seed=1003 + 7919 * i + 100003 * rank) for i in range(n)]
+    return wl.prefill_paged_sets(n, seed=1003 + 100003 * rank)
 
 
 def run_ours(args):
@@ -400,15 +406,18 @@ def run_ours(args):
         calls[w % R]()
     torch.cuda.synchronize()
 
-    # ---- graphs: one full rotation, plus the remainder; each replayed once untimed ----
+    # ---- graphs of GRAPH_CALLS calls (a multiple of R), plus the remainder;
+    # each replayed once untimed. Calls overlap (programmatic dependent
+    # launch) only inside a graph, so graphs are long. ----
     K = args.steps
-    full, rem = divmod(K, R)
+    G = min(GRAPH_CALLS, K) // R * R or K
+    full, rem = divmod(K, G)
     graphs = []
-    for n in ([R] if full else []) + ([rem] if rem else []):
+    for n in ([G] if full else []) + ([rem] if rem else []):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(n):
-                calls[i]()
+                calls[i % R]()
         graphs.append(g)
     for g in graphs:
         g.replay()           # graph upload and first-launch costs stay out of the timed region
@@ -425,6 +434,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    hold_stream()            # before e0: the host enqueues the graphs while the GPU spins
     wall0 = time.time()
     e0.record(stream)
     for _ in range(full):
@@ -468,7 +478,8 @@ def run_ours(args):
                        "l2": "inputs larger than L2: steps rotate over %d input sets (%.0f MB > %.0f MB L2)"
                              % (R, in_mb, l2 / 1e6),
                        "launch": "CUDA graph replays of back-to-back calls (%d x %d-step graph + %d-step "
-                                 "graph, each replayed once untimed first)" % (full, R, rem),
+                                 "graph, each replayed once untimed first; a 1 ms device spin before the start "
+                                 "event hides the host's launch latency)" % (full, G, rem),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -553,6 +564,15 @@ def e2e_prefill(args, cases, gamma, ckv, kc, dev, kvr):
                    "one stream, synchronised after the K steps"}
 
 
+def hold_stream(ms=1.0):
+    """Keep the current stream busy for about `ms` milliseconds (a device-side
+    spin, no memory traffic), so that the host has enqueued what follows
+    before the GPU reaches it: the start event then times the GPU work, not
+    the host's graph-launch latency."""
+    import torch
+    torch.cuda._sleep(int(ms * 2e6))   # cycles at ~2 GHz
+
+
 def time_graph(calls, n_calls, stream):
     """Average duration of one call when n_calls calls (cycling through
     `calls`) run back to back as one CUDA graph replay (after one untimed
@@ -566,6 +586,7 @@ def time_graph(calls, n_calls, stream):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    hold_stream()
     e0.record(stream)
     g.replay()
     e1.record(stream)
@@ -764,19 +785,42 @@ def run_only(args):
         sc = torch.empty(q.shape[:-1] + (1,), dtype=torch.float32, device=dev)
         ex = args.only == "dynamic_quant_decode_exact"
         fn = lambda: kvr.dynamic_quant(q, o, sc, exact=ex)
+    elif args.only == "decode_paged":
+        # the decode batches the extras rotate through (512 sets, larger than L2)
+        sets = wl.decode_paged_sets(512, seed=1002)
+        ckv = torch.zeros(sets["d0"], sets["d1"], 1, 512, dtype=torch.bfloat16, device=dev)
+        kc = torch.zeros(sets["d0"], sets["d1"], 1, 64, dtype=torch.bfloat16, device=dev)
+        kv, cs, sn, ix = (sets[k].to(dev) for k in ("kv", "cos", "sin", "index"))
+        gamma = sets["gamma"].to(dev)
+        calls = [kvr.prepare_kv_rmsnorm_rope_cache(kv[i], gamma, cs[i], sn[i], ix[i], ckv, kc, cache_mode="PA_BSND")
+                 for i in range(512)]
+        it = iter(range(1 << 62))
+        fn = lambda: calls[next(it) % len(calls)]()
     else:
-        case = getattr(wl, args.only)()
+        # prefill: the benchmark's rotation of input sets (larger than L2); others: one set
+        cases = prefill_sets(ROTATION) if args.only == "prefill_paged" else [getattr(wl, args.only)()]
+        case = cases[0]
         ckv = torch.zeros(case.cache_shapes()[0], dtype=wl.code_torch_dtype(case.ckv_dtype), device=dev).view(
             wl.TORCH_DTYPES[case.ckv_dtype])
         kc = torch.zeros(case.cache_shapes()[1], dtype=wl.code_torch_dtype(case.k_dtype), device=dev).view(
             wl.TORCH_DTYPES[case.k_dtype])
-        a = (case.kv.to(dev), case.gamma.to(dev), case.cos.to(dev), case.sin.to(dev), case.index.to(dev), ckv, kc)
-        kw = dict(cache_mode=case.mode, eps=case.eps,
-                  ckv_scale=None if case.ckv_scale is None else case.ckv_scale.to(dev))
-        fn = lambda: kvr.kv_rmsnorm_rope_cache(*a, **kw)
+        calls = [kvr.prepare_kv_rmsnorm_rope_cache(
+            c.kv.to(dev), case.gamma.to(dev), c.cos.to(dev), c.sin.to(dev), c.index.to(dev), ckv, kc,
+            cache_mode=c.mode, eps=c.eps, ckv_scale=None if c.ckv_scale is None else c.ckv_scale.to(dev))
+            for c in cases]
+        it = iter(range(1 << 62))
+        fn = lambda: calls[next(it) % len(calls)]()
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
+    if args.profile_range:
+        cudart = torch.cuda.cudart()
+        cudart.cudaProfilerStart()
+        for _ in range(args.steps):
+            fn()
+        cudart.cudaProfilerStop()
+        torch.cuda.synchronize()
+        return {"only": args.only, "launches": args.warmup + args.steps, "range": args.steps}
     stream = torch.cuda.current_stream()
     ts = []
     for _ in range(args.steps):

@@ -95,3 +95,19 @@ def test_algorithmic_bytes_of_the_workloads():
     assert bench.kv_algorithmic_bytes(4096, 0, ckv_bytes=1, scale_bytes=2048) == 4096 * 2056 + 1024 + 2048
     assert bench.qsa_algorithmic_bytes(1024, 32, 64, 128, 64) == 1024 * (16384 + 256 + 256) + 256 + 256 == 17302016
     assert bench.dq_algorithmic_bytes(32768, 512) == 32768 * 1540 == 50462720
+
+
+def test_prefill_rotation_writes_disjoint_rows():
+    """The benchmark's rotated prefill batches write disjoint cache blocks,
+    each batch 32768 distinct slots, contiguous within each 128-slot block:
+    no call rewrites a row another call of the rotation wrote."""
+    import torch
+    from attention_prologue_kv_gb300 import workloads as wl
+    cases = bench.prefill_sets(bench.ROTATION)
+    blocks = [set((c.index // 128).tolist()) for c in cases]
+    assert all(len(b) == 256 for b in blocks)
+    assert len(set.union(*blocks)) == 256 * len(cases)
+    for c in cases:
+        idx = c.index.view(8, 4096)
+        assert len(set(c.index.tolist())) == 32768
+        assert torch.all((idx[:, 1:] - idx[:, :-1])[:, torch.arange(4095) % 128 != 127] == 1)
