@@ -772,13 +772,16 @@ def run_only(args):
     build()
     dev = torch.device("cuda", 0)
     if args.only in ("qsa_prepare", "qsa_prepare_params_ready"):
-        q = wl.qsa_prepare_workload()
-        bk = torch.zeros(q.N, q.Bcap, q.Di, dtype=torch.bfloat16, device=dev)
+        # the input sets the extras rotate through (together larger than L2)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        qs = [wl.qsa_prepare_workload(seed=1005 + 7919 * i) for i in range(max(3, int(2 * l2 // 17.3e6) + 1))]
+        bk = torch.zeros(qs[0].N, qs[0].Bcap, qs[0].Di, dtype=torch.bfloat16, device=dev)
         d = lambda t: t.to(dev)
-        a = (d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
-             d(q.past_raw), d(q.past_rope), q.kbs, q.eps)
+        args_q = [(d(q.raw), bk, d(q.key_length), d(q.rope_cos), d(q.rope_sin), d(q.k_norm_weight),
+                   d(q.past_raw), d(q.past_rope), q.kbs, q.eps) for q in qs]
         pr = args.only == "qsa_prepare_params_ready"
-        fn = lambda: kvr.qsa_prepare(*a, params_ready=pr)
+        it = iter(range(1 << 62))
+        fn = lambda: kvr.qsa_prepare(*args_q[next(it) % len(args_q)], params_ready=pr)
     elif args.only in ("dynamic_quant_decode", "dynamic_quant_decode_exact"):
         q = wl.dynamic_quant_decode().to(dev)
         o = torch.empty(q.shape, dtype=torch.int8, device=dev)

@@ -206,6 +206,61 @@ def test_large_ragged_grid_stride():
     check(case)
 
 
+BULK_CASES = {
+    # (Bkv, Skv, make_kv_case keywords): every case has >= 8192 rows (the pipeline kernel)
+    "threshold_8192": (1, 8192, dict(mode="PA_BSND", d0=80, d1=128, skip=17)),
+    "odd_8193": (1, 8193, dict(mode="PA_BSND", d0=80, d1=128, skip=3)),
+    "norm_odd": (3, 6667, dict(mode="Norm", d0=4, d1=6700, skip=11)),
+    "blk_bsnd": (5, 2000, dict(mode="PA_BLK_BSND", d0=5 * 16 + 3, d1=128)),
+    "fp8_per_channel": (2, 5003, dict(mode="PA_BSND", d0=100, d1=128, ckv_dtype="fp8_e4m3fn", kv_std=3.0)),
+    "int8_e5m2_per_tensor": (2, 4500, dict(mode="PA_BSND", d0=80, d1=128, ckv_dtype="int8", k_dtype="fp8_e5m2",
+                                            scale_len=1, k_scale_len=1, kv_std=3.0)),
+    "strided_rows": (4, 2500, dict(mode="PA_BSND", d0=90, d1=128, row_pad=64, skip=9)),
+    "f16": (2, 4200, dict(mode="PA_BSND", d0=80, d1=128, in_dtype="f16", ckv_dtype="f16", k_dtype="f16")),
+    "other_split": (2, 4600, dict(mode="PA_BSND", Dv=256, Dk=32, d0=80, d1=128, skip=5)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BULK_CASES))
+def test_bulk_pipeline_paths(name):
+    """The bulk-copy pipeline (batches of 8192 rows or more): each SM's row
+    range, ragged last tiles, per-row copies of strided rows, index entries
+    read from global memory (PA_BLK_BSND), 8-bit codes, f16 and another row
+    split, against the oracle."""
+    Bkv, Skv, kw = BULK_CASES[name]
+    case = wl.make_kv_case("bulk_" + name, Bkv, Skv, seed=7000 + len(name), **kw)
+    assert case.T >= 8192
+    n, _, _ = check(case)
+    assert n == case.active_tokens()
+
+
+def test_bulk_pipeline_misaligned_index_and_bad_entries():
+    """An index buffer at an 8-byte (not 16-byte) offset takes the global
+    index reads; out-of-range entries are skipped and flagged."""
+    import attention_prologue_kv_gb300 as kvr
+    case = wl.make_kv_case("bulk_idx", 2, 4800, mode="PA_BSND", d0=80, d1=128, seed=7100, skip=7)
+    case.index[5] = 80 * 128
+    case.index[9000] = -3
+    ref_ckv, ref_k, ref_st = run_oracle_kv(case)
+    assert ref_st == 1
+    buf = torch.empty(case.T + 1, dtype=torch.int64, device="cuda")
+    idx = buf[1:]
+    idx.copy_(case.index)
+    assert idx.data_ptr() % 16 == 8
+    ckv, c1 = guarded_cache(case.cache_shapes()[0], "bf16")
+    k, c2 = guarded_cache(case.cache_shapes()[1], "bf16")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvr.kv_rmsnorm_rope_cache(case.kv.cuda(), case.gamma.cuda(), case.cos.cuda(), case.sin.cuda(), idx, ckv, k,
+                              cache_mode="PA_BSND", eps=case.eps, dev_status=status)
+    torch.cuda.synchronize()
+    c1()
+    c2()
+    assert int(status.item()) == ref_st
+    n1, _ = compare_cache(codes_of(ckv), ref_ckv, "bf16", case.Dv)
+    n2, _ = compare_cache(codes_of(k), ref_k, "bf16", case.Dk)
+    assert n1 == n2 == case.active_tokens() - 2
+
+
 def test_rope_identity_on_gpu_is_exact_deinterleave():
     case = wl.make_kv_case("i", 2, 8, mode="PA_BSND", d0=1, d1=16, seed=55)
     case.cos[:] = 1.0
