@@ -19,7 +19,7 @@ hand-worked toys (tests/golden) or library routines; no part is
 """
 from . import encoders
 from .kv_rmsnorm_rope_cache import (NORM, PA_BLK_BSND, PA_BSND, STATUS_INDEX,
-                                    cache_slot, interleave_rope, quantise,
+                                    cache_slot, interleave_rope, kv_values, quantise,
                                     ref_kv_rmsnorm_rope_cache,
                                     ref_kv_rmsnorm_rope_cache_loop, rms_norm)
 from .qsa_prepare import (ROPE_LAYOUTS, STATUS_BLOCK_CAP, STATUS_KEY_LENGTH,
@@ -28,7 +28,7 @@ from .dynamic_quant import ref_dynamic_quant
 
 __all__ = [
     "encoders", "NORM", "PA_BSND", "PA_BLK_BSND", "STATUS_INDEX", "STATUS_KEY_LENGTH",
-    "STATUS_BLOCK_CAP", "STATUS_PAST_BLOCKS", "ROPE_LAYOUTS", "rotate_half_rope", "cache_slot", "interleave_rope", "quantise", "rms_norm",
+    "STATUS_BLOCK_CAP", "STATUS_PAST_BLOCKS", "ROPE_LAYOUTS", "rotate_half_rope", "cache_slot", "interleave_rope", "kv_values", "quantise", "rms_norm",
     "ref_kv_rmsnorm_rope_cache", "ref_kv_rmsnorm_rope_cache_loop", "ref_qsa_prepare",
     "ref_dynamic_quant",
 ]

@@ -76,6 +76,28 @@ def quantise(y, dtype, scale):
     return enc.encode(y * np.asarray(scale, dtype=np.float64), dtype)
 
 
+def kv_values(kv, gamma, cos, sin, *, Dv, eps, ckv_scale=None, k_scale=None, kc_scale=1.0):
+    """The float64 value each cache element encodes before its one rounding,
+    per token: (vy [.., Dv], vr [.., Dk], mr [.., Dk]). vy = alpha * rmsNorm
+    (times the ckv scale for an 8-bit cache), vr = interleaveRope (times the
+    k scale), and mr = the sum of the magnitudes of the two RoPE terms behind
+    each vr element (times |k scale|): a bound for the size of the terms a
+    finite-precision evaluation of vr rounds, which can exceed |vr| by far
+    when the terms cancel."""
+    y = float(kc_scale) * rms_norm(kv[..., :Dv], gamma, float(eps))
+    z = kv[..., Dv:]
+    r = interleave_rope(z, cos, sin)
+    zeros = np.zeros_like(cos)
+    m = interleave_rope(np.abs(z), np.abs(cos), zeros) + np.abs(interleave_rope(np.abs(z), zeros, np.abs(sin)))
+    if ckv_scale is not None:
+        y = y * np.asarray(ckv_scale, dtype=np.float64)
+    if k_scale is not None:
+        ks = np.asarray(k_scale, dtype=np.float64)
+        r = r * ks
+        m = m * np.abs(ks)
+    return y, r, m
+
+
 def cache_slot(mode, b, s, index, Skv, d0, d1):
     """Where token (b, s) goes: returns None (skip), "bad" (index out of
     range: skipped, status raised) or the (row0, row1) cache coordinates.

@@ -79,14 +79,20 @@ def rotate_channels(u, c, s, layout):
 def ref_qsa_prepare(raw, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,
                     past_raw, past_rope, key_block_size, eps=1e-6,
                     next_raw=None, next_rope=None, out_dtype="bf16",
-                    rope_layout="interleave_last", past_block_keys=None):
+                    rope_layout="interleave_last", past_block_keys=None, values_out=None):
     """raw [N, L, Di] f64; block_keys codes [N, Bcap, Di] (written in place);
     key_length int [N] or [1]; rope_cos/rope_sin [N, L, Dr] f64 or None;
     k_norm_weight [Di] f64 or None; past_raw [N, kbs-1, Di] f64;
     past_rope [N, 2*Dr] f64 or None; next_raw [N, kbs-1, Di] f64 / next_rope
     [N, 2*Dr] f64 optional carry outputs (written in place); rope_layout
     one of ROPE_LAYOUTS; past_block_keys codes [N, Bp, Di] or None (None:
-    block_keys already holds the past keys).
+    block_keys already holds the past keys). values_out: optional dict that
+    receives, for every block key written, (n, j) -> (u, b): the float64 key
+    before its rounding, and per element a bound on the magnitudes of the
+    terms summed into it (the same steps applied to the mean of |key|, with
+    the normalisation factor of the true mean and the magnitudes of both
+    rotation terms), for judging how far a finite-precision evaluation may
+    stray.
     Returns the device-status bits the call would raise."""
     if rope_layout not in ROPE_LAYOUTS:
         raise ValueError(rope_layout)
@@ -123,15 +129,24 @@ def ref_qsa_prepare(raw, block_keys, key_length, rope_cos, rope_sin, k_norm_weig
             return past_rope[n, :Dr], past_rope[n, Dr:]
 
         for j in range(P // kbs, K // kbs):
-            m = np.mean(np.stack([key(p) for p in range(j * kbs, (j + 1) * kbs)]), axis=0)
+            rows = np.stack([key(p) for p in range(j * kbs, (j + 1) * kbs)])
+            m = np.mean(rows, axis=0)
             u = m if k_norm_weight is None else rms_norm(m, k_norm_weight, eps)
+            bound = np.mean(np.abs(rows), axis=0)
+            if k_norm_weight is not None:   # the same normalisation factor, on magnitudes
+                bound = bound * np.abs(k_norm_weight) / np.sqrt(np.mean(m * m) + eps)
             if rope_cos is not None:
                 c, s = rope_at(j * kbs)
                 u = rotate_channels(u, c, s, rope_layout)
+                zero = np.zeros_like(c)
+                bound = rotate_channels(bound, np.abs(c), zero, rope_layout) + np.abs(
+                    rotate_channels(bound, zero, np.abs(s), rope_layout))
             if j >= Bcap:
                 status |= STATUS_BLOCK_CAP
                 continue
             block_keys[n, j] = enc.encode(u, out_dtype)
+            if values_out is not None:
+                values_out[(n, j)] = (u, bound)
 
         Fn = (K // kbs) * kbs
         if next_raw is not None:

@@ -76,6 +76,62 @@ def run_oracle_kv(case, ckv=None, k=None, loop=False):
     return ckv, k, st
 
 
+ROBUST_REL = 2.0 ** -17   # perturbation within which a float32 evaluation may land on either side
+
+
+def robust_codes(v, margin, dtype):
+    """(codes of v, mask): the mask marks elements whose code does not change
+    anywhere in [v - margin, v + margin] (the encoders are monotone, so the
+    ends decide), i.e. elements no evaluation within that error can round
+    differently."""
+    from oracle import encoders as enc
+    want = enc.encode(v, dtype)
+    return want, enc.encode(v - margin, dtype) == enc.encode(v + margin, dtype)
+
+
+def kv_token_rows(case):
+    """Flat cache row of every token the oracle writes, and its (b, s)."""
+    import oracle
+    index = case.index.numpy()
+    rows, bs, ss = [], [], []
+    for b in range(case.Bkv):
+        for s in range(case.Skv):
+            slot = oracle.cache_slot(case.mode, b, s, index, case.Skv, case.d0, case.d1)
+            if isinstance(slot, tuple):
+                rows.append(slot[0] * case.d1 + slot[1])
+                bs.append(b)
+                ss.append(s)
+    return np.array(rows, dtype=np.int64), np.array(bs, dtype=np.int64), np.array(ss, dtype=np.int64)
+
+
+def check_robust_kv(case, g_ckv, g_k, rel=ROBUST_REL):
+    """Codes bit-identical to the oracle's wherever the oracle's float64 value
+    lies farther than `rel` (relative; for the RoPE part relative to the
+    size of its terms) from a rounding boundary of the cache type: a wrong
+    rounding mode or a systematic error of one unit fails here even though it
+    stays within the one-ulp / one-code tolerance. Returns the fraction of
+    written elements checked."""
+    import oracle
+    kv, gamma, cos, sin, _ = oracle_kv_inputs(case)
+    vy, vr, mr = oracle.kv_values(
+        kv, gamma, cos, sin, Dv=case.Dv, eps=f32_arg(case.eps),
+        ckv_scale=None if case.ckv_scale is None else case.ckv_scale.numpy(),
+        k_scale=None if case.k_scale is None else case.k_scale.numpy(), kc_scale=f32_arg(case.kc_scale))
+    rows, bs, ss = kv_token_rows(case)
+    checked, total = 0, 0
+    for g, v, m, dt, width in ((g_ckv, vy, None, case.ckv_dtype, case.Dv), (g_k, vr, mr, case.k_dtype, case.Dk)):
+        gv = np.asarray(g).reshape(-1, width)[rows]
+        vt = v[bs, ss]
+        margin = rel * (np.abs(vt) if m is None else m[bs, ss])
+        want, robust = robust_codes(vt, margin, dt)
+        bad = robust & (gv != want)
+        assert not bad.any(), "%d codes differ from the oracle away from any rounding boundary (%s), e.g. gpu %s want %s" % (
+            int(bad.sum()), dt, gv[bad][:4], want[bad][:4])
+        checked += int(robust.sum())
+        total += robust.size
+    return checked / total if total else 1.0
+
+
 def oracle_qsa_inputs(case):
     return dict(raw=f64(case.raw), key_length=case.key_length.numpy(),
                 rope_cos=f64(case.rope_cos), rope_sin=f64(case.rope_sin),
@@ -84,8 +140,9 @@ def oracle_qsa_inputs(case):
 
 
 def run_oracle_qsa(case, block_keys=None, carry=False, rope_layout="interleave_last",
-                   past_block_keys=None):
-    """past_block_keys: codes [N, Bp, Di] (numpy) for the concat-output form."""
+                   past_block_keys=None, values_out=None):
+    """past_block_keys: codes [N, Bp, Di] (numpy) for the concat-output form;
+    values_out: dict receiving the oracle's pre-rounding keys (see ref_qsa_prepare)."""
     import oracle
     from attention_prologue_kv_gb300.workloads import SENTINEL16
     if block_keys is None:
@@ -96,9 +153,29 @@ def run_oracle_qsa(case, block_keys=None, carry=False, rope_layout="interleave_l
         npr = np.full((case.N, 2 * case.Dr), np.nan) if case.Dr else None
     st = oracle.ref_qsa_prepare(block_keys=block_keys, next_raw=nr, next_rope=npr,
                                 rope_layout=rope_layout, past_block_keys=past_block_keys,
+                                values_out=values_out,
                                 out_dtype="f16" if case.raw.dtype == torch.float16 else "bf16",
                                 **oracle_qsa_inputs(case))
     return block_keys, nr, npr, st
+
+
+QSA_ROBUST_REL = 2.0 ** -17   # float32 error of the block sum and the rotation: at most ~2**-18 of the terms
+
+
+def check_robust_qsa(g_bk, values, dtype, rel=QSA_ROBUST_REL):
+    """Block keys bit-identical to the oracle's wherever its float64 key lies
+    farther than `rel` times the magnitude bound of its terms from a rounding
+    boundary (values: the oracle's values_out). Returns the fraction checked."""
+    checked, total = 0, 0
+    for (n, j), (u, b) in values.items():
+        want, robust = robust_codes(u, rel * b, dtype)
+        got = np.asarray(g_bk)[n, j]
+        bad = robust & (got != want)
+        assert not bad.any(), "block (%d, %d): %d elements differ away from any rounding boundary" % (
+            n, j, int(bad.sum()))
+        checked += int(robust.sum())
+        total += robust.size
+    return checked / total if total else 1.0
 
 
 # ---------------------------------------------------------------------------

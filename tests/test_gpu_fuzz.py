@@ -12,8 +12,8 @@ import pytest
 import torch
 
 from attention_prologue_kv_gb300 import workloads as wl
-from helpers import (compare_cache, compare_dynamic_quant, run_gpu_kv, run_gpu_qsa, run_oracle_kv,
-                     run_oracle_qsa)
+from helpers import (check_robust_kv, check_robust_qsa, compare_cache, compare_dynamic_quant, run_gpu_kv,
+                     run_gpu_qsa, run_oracle_kv, run_oracle_qsa)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +55,8 @@ def test_kv_random_configurations(i):
     n1, _ = compare_cache(g_ckv, ref_ckv, case.ckv_dtype, case.Dv)
     n2, _ = compare_cache(g_k, ref_k, case.k_dtype, case.Dk)
     assert n1 == n2 == case.active_tokens(), cfg
+    if n1:
+        check_robust_kv(case, g_ckv, g_k)
 
 
 def qsa_config(i):
@@ -84,10 +86,12 @@ def test_qsa_random_configurations(i):
         Bp = max(0, j0max + opt["bp_extra"])
         past_bk = np.random.default_rng(i).integers(0, 0x7C00, (case.N, Bp, case.Di), dtype=np.uint16)
     kw = dict(carry=opt["carry"], rope_layout=opt["rope_layout"], past_block_keys=past_bk)
-    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
+    values = {}
+    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, values_out=values, **kw)
     g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=opt["params_ready"], **kw)
     assert g_st == r_st, (cfg, opt)
     compare_cache(g_bk, r_bk, "bf16" if cfg["in_dtype"] == "bf16" else "f16", case.Di)
+    check_robust_qsa(g_bk, values, "bf16" if cfg["in_dtype"] == "bf16" else "f16")
     if opt["carry"]:
         assert np.array_equal(g_nr, r_nr, equal_nan=True)
         if case.Dr:
@@ -125,6 +129,8 @@ def test_kv_random_configurations_compiled_split(i):
     n1, _ = compare_cache(g_ckv, ref_ckv, case.ckv_dtype, case.Dv)
     n2, _ = compare_cache(g_k, ref_k, case.k_dtype, case.Dk)
     assert n1 == n2 == case.active_tokens(), cfg
+    if n1:
+        check_robust_kv(case, g_ckv, g_k)
 
 
 @pytest.mark.parametrize("i", range(20))
@@ -141,10 +147,12 @@ def test_qsa_random_configurations_compiled_shapes(i):
         Bp = max(0, int(((K - case.L) // case.kbs).max()) + opt["bp_extra"])
         past_bk = np.random.default_rng(i).integers(0, 0x7C00, (case.N, Bp, case.Di), dtype=np.uint16)
     kw = dict(carry=opt["carry"], rope_layout=opt["rope_layout"], past_block_keys=past_bk)
-    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
+    values = {}
+    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, values_out=values, **kw)
     g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=opt["params_ready"], **kw)
     assert g_st == r_st, (cfg, opt)
     compare_cache(g_bk, r_bk, "bf16" if cfg["in_dtype"] == "bf16" else "f16", case.Di)
+    check_robust_qsa(g_bk, values, "bf16" if cfg["in_dtype"] == "bf16" else "f16")
     if opt["carry"]:
         assert np.array_equal(g_nr, r_nr, equal_nan=True)
         if case.Dr:

@@ -1,7 +1,8 @@
 """GPU parity of kv_rmsnorm_rope_cache against the float64 oracle on the same
 seeded inputs: every cache byte outside the indexed rows bit-exact, 16-bit
-outputs within 2**-7*|ref| + 1e-6, 8-bit codes within one code; device
-status bits equal. Covers the four KV workloads at full size, both kernel
+outputs within 2**-7*|ref| + 1e-6, 8-bit codes within one code, and every
+code bit-identical to the oracle's wherever its float64 value lies farther
+than 2**-17 (relative) from a rounding boundary; device status bits equal. Covers the four KV workloads at full size, both kernel
 paths (vectorised and generic), every cache mode and code type, strided and
 misaligned rows, and the degenerate cases."""
 import numpy as np
@@ -9,7 +10,8 @@ import pytest
 import torch
 
 from attention_prologue_kv_gb300 import workloads as wl
-from helpers import codes_of, compare_cache, guarded_cache, run_gpu_kv, run_oracle_kv, sentinel_cache
+from helpers import (check_robust_kv, codes_of, compare_cache, guarded_cache, run_gpu_kv, run_oracle_kv,
+                     sentinel_cache)
 
 pytestmark = pytest.mark.gpu
 
@@ -21,6 +23,8 @@ def check(case, **kw):
     n1, ex1 = compare_cache(g_ckv, ref_ckv, case.ckv_dtype, case.Dv)
     n2, ex2 = compare_cache(g_k, ref_k, case.k_dtype, case.Dk)
     assert n1 == n2
+    if n1:
+        check_robust_kv(case, g_ckv, g_k)
     return n1, ex1, ex2
 
 

@@ -7,14 +7,15 @@ import pytest
 import torch
 
 from attention_prologue_kv_gb300 import workloads as wl
-from helpers import compare_cache, run_gpu_qsa, run_oracle_qsa
+from helpers import check_robust_qsa, compare_cache, run_gpu_qsa, run_oracle_qsa
 
 pytestmark = pytest.mark.gpu
 
 
 def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None, params_ready=False):
     kw = dict(carry=carry, rope_layout=rope_layout, past_block_keys=past_block_keys)
-    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, **kw)
+    values = {}
+    r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, values_out=values, **kw)
     g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=params_ready, **kw)
     assert g_st == r_st
     if past_block_keys is not None:
@@ -23,6 +24,7 @@ def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None,
             m = min(past_block_keys.shape[1], P // case.kbs, case.Bcap)
             assert np.array_equal(g_bk[n, :m], r_bk[n, :m])
     n, exact = compare_cache(g_bk, r_bk, "bf16", case.Di)
+    check_robust_qsa(g_bk, values, "bf16")
     if carry:
         assert np.array_equal(g_nr, r_nr, equal_nan=True)
         if case.Dr:

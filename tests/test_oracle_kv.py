@@ -251,3 +251,56 @@ def test_untouched_slots_keep_any_prior_contents():
     assert np.array_equal(k.reshape(-1, case.Dk)[mask], k0.reshape(-1, case.Dk)[mask])
     assert not np.array_equal(ckv.reshape(-1, case.Dv)[live], ckv0.reshape(-1, case.Dv)[live])
     assert (idx == -1).sum() == 5
+
+
+def _robust_case(ckv_dtype, k_dtype):
+    from attention_prologue_kv_gb300 import workloads as wl
+    return wl.make_kv_case("rb", 3, 40, Dv=64, Dk=16, mode="PA_BSND", d0=4, d1=64, seed=91, skip=4,
+                           ckv_dtype=ckv_dtype, k_dtype=k_dtype, kv_std=3.0)
+
+
+def _encode_like_gpu(case, enc_fn):
+    """Caches holding enc_fn(float32 evaluation of the oracle's values), at
+    the oracle's rows: a stand-in for a GPU result, built on the CPU."""
+    import oracle
+    from helpers import f32_arg, kv_token_rows, oracle_kv_inputs, sentinel_caches_np
+    kv, gamma, cos, sin, _ = oracle_kv_inputs(case)
+    f32 = lambda a: None if a is None else np.asarray(a, dtype=np.float32)
+    vy, vr, _ = oracle.kv_values(f32(kv), f32(gamma), f32(cos), f32(sin), Dv=case.Dv, eps=np.float32(f32_arg(case.eps)),
+                                 ckv_scale=None if case.ckv_scale is None else case.ckv_scale.numpy(),
+                                 k_scale=None if case.k_scale is None else case.k_scale.numpy())
+    ckv, k = sentinel_caches_np(case)
+    rows, bs, ss = kv_token_rows(case)
+    ckv.reshape(-1, case.Dv)[rows] = enc_fn(vy[bs, ss].astype(np.float64), case.ckv_dtype)
+    k.reshape(-1, case.Dk)[rows] = enc_fn(vr[bs, ss].astype(np.float64), case.k_dtype)
+    return ckv, k
+
+
+@pytest.mark.parametrize("dtypes", [("bf16", "bf16"), ("fp8_e4m3fn", "int8"), ("int8", "fp8_e5m2")])
+def test_robust_check_accepts_float32_and_rejects_truncation(dtypes):
+    """The exactness check used by the GPU parity tests: a float32 evaluation
+    of the method, rounded like the oracle, passes (and most elements are
+    checked); the same values encoded by truncation toward zero fail it,
+    although they stay within one ulp / one code of the oracle."""
+    from oracle import encoders as enc
+    from helpers import check_robust_kv
+    case = _robust_case(*dtypes)
+    good_ckv, good_k = _encode_like_gpu(case, enc.encode)
+    assert check_robust_kv(case, good_ckv, good_k) > 0.95
+
+    def trunc(v, dt):
+        if dt == "int8":
+            return enc.encode(np.trunc(v), dt)
+        # step toward zero: the largest code magnitude not above |v|
+        c = enc.encode(v, dt)
+        back = enc.decode(c, dt)
+        over = np.abs(back) > np.abs(v)
+        ordn = enc.code_ordinal(c, dt)
+        ordn = np.where(over, ordn - np.sign(ordn), ordn)
+        mag = np.abs(ordn)
+        width = 16 if dt in enc.DTYPES_16 else 8
+        signbit = np.where(ordn < 0, 1 << (width - 1), 0)
+        return (mag | signbit).astype(enc.code_dtype(dt))
+    bad_ckv, bad_k = _encode_like_gpu(case, trunc)
+    with pytest.raises(AssertionError, match="away from any rounding boundary"):
+        check_robust_kv(case, bad_ckv, bad_k)

@@ -256,3 +256,31 @@ def test_concat_form_past_beyond_capacity_raises_block_cap():
     bk, _, _, st = run_oracle_qsa(case, past_block_keys=past)
     assert st == oracle.STATUS_BLOCK_CAP
     assert np.array_equal(bk[0], past[0, :3])
+
+
+@pytest.mark.parametrize("layout", ["interleave_last", "half_first"])
+def test_robust_check_accepts_float32_and_rejects_truncation(layout):
+    """The block-key exactness check used by the GPU parity tests: the same
+    steps evaluated in float32 and rounded like the oracle pass (with most
+    elements checked); truncating the float64 keys toward zero fails,
+    although it stays within one ulp."""
+    from attention_prologue_kv_gb300 import workloads as wl
+    from helpers import check_robust_qsa, oracle_qsa_inputs
+    from oracle import encoders as enc
+    case = wl.make_qsa_case("rb", 3, 300, Di=64, Dr=32, kbs=32, seed=77, past_max=200)
+    values = {}
+    bk64 = np.full((case.N, case.Bcap, case.Di), 0x7FBF, dtype=np.uint16)
+    oracle.ref_qsa_prepare(block_keys=bk64, values_out=values, rope_layout=layout, **oracle_qsa_inputs(case))
+    assert len(values) > 10
+    inp = {k: (v.astype(np.float32) if isinstance(v, np.ndarray) and v.dtype == np.float64 else v)
+           for k, v in oracle_qsa_inputs(case).items()}
+    bk32 = np.full_like(bk64, 0x7FBF)
+    oracle.ref_qsa_prepare(block_keys=bk32, rope_layout=layout, **inp)
+    assert check_robust_qsa(bk32, values, "bf16") > 0.85
+    bad = bk64.copy()
+    for (n, j), (u, _) in values.items():
+        c = enc.bf16_encode(u)
+        over = np.abs(enc.bf16_decode(c)) > np.abs(u)
+        bad[n, j] = np.where(over, c - 1, c)          # one step toward zero in magnitude
+    with pytest.raises(AssertionError, match="away from any rounding boundary"):
+        check_robust_qsa(bad, values, "bf16")
