@@ -20,7 +20,8 @@
 //    bulk copy for the kv rows (one per row when rows are strided), one for
 //    the cos rows, one for the sin rows and one for the index entries, all
 //    completing on the stage's `full` mbarrier (expect_tx byte count);
-//  * S stages in flight per SM (S*R rows, ~100-160 KB), recycled through an
+//  * S stages in flight per SM (S*R rows, up to 200 KB: 4 stages of 32 rows
+//    for the 512 + 64 split), recycled through an
 //    `empty` mbarrier that each consumer warp arrives on;
 //  * a consumer warp owns one row at a time: 16-byte shared loads of the Dv
 //    part (conflict-free), fp32 sum of squares with a warp butterfly, gamma
