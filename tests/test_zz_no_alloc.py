@@ -21,7 +21,7 @@ import torch
 
 from attention_prologue_kv_gb300 import _native as N
 from attention_prologue_kv_gb300 import workloads as wl
-from helpers import codes_of, compare_cache, run_oracle_kv, sentinel_cache
+from helpers import check_robust_kv, codes_of, compare_cache, run_oracle_kv, sentinel_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -95,6 +95,7 @@ def test_static_staging_matches_the_staged_call_twice_in_a_row():
         n1, _ = compare_cache(codes_of(ckv), r_ckv, "bf16", 512)
         n2, _ = compare_cache(codes_of(k), r_k, "bf16", 64)
         assert n1 == n2 == rows_after[i]
+        check_robust_kv((a, b)[i], codes_of(ckv), codes_of(k))   # this call's rows, exact away from ties
     assert int(st.item()) == int(st_ref.item()) == N.KVR_DEVERR_INDEX
 
 
