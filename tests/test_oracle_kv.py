@@ -304,3 +304,27 @@ def test_robust_check_accepts_float32_and_rejects_truncation(dtypes):
     bad_ckv, bad_k = _encode_like_gpu(case, trunc)
     with pytest.raises(AssertionError, match="away from any rounding boundary"):
         check_robust_kv(case, bad_ckv, bad_k)
+
+
+@pytest.mark.parametrize("dtypes", [("bf16", "bf16"), ("fp8_e4m3fn", "int8"), ("f16", "fp8_e5m2")])
+def test_kv_values_encode_to_the_oracle_caches(dtypes):
+    """kv_values (the float64 value each element encodes) agrees with the
+    oracle: encoding it gives the written rows code for code, and the RoPE
+    magnitude bound dominates the value."""
+    from oracle import encoders as enc
+    from helpers import f32_arg, kv_token_rows, oracle_kv_inputs, run_oracle_kv
+    from attention_prologue_kv_gb300 import workloads as wl
+    in_dtype = "f16" if dtypes[0] == "f16" else "bf16"
+    case = wl.make_kv_case("kvv", 3, 30, Dv=48, Dk=24, mode="PA_BSND", d0=4, d1=32, seed=93, skip=5,
+                           ckv_dtype=dtypes[0], k_dtype=dtypes[1], in_dtype=in_dtype, kc_scale=0.8)
+    ref_ckv, ref_k, _ = run_oracle_kv(case)
+    kv, gamma, cos, sin, _ = oracle_kv_inputs(case)
+    vy, vr, mr = oracle.kv_values(kv, gamma, cos, sin, Dv=case.Dv, eps=f32_arg(case.eps),
+                                  ckv_scale=None if case.ckv_scale is None else case.ckv_scale.numpy(),
+                                  k_scale=None if case.k_scale is None else case.k_scale.numpy(),
+                                  kc_scale=f32_arg(case.kc_scale))
+    rows, bs, ss = kv_token_rows(case)
+    assert len(rows) == case.active_tokens()
+    assert np.array_equal(enc.encode(vy[bs, ss], case.ckv_dtype), ref_ckv.reshape(-1, case.Dv)[rows])
+    assert np.array_equal(enc.encode(vr[bs, ss], case.k_dtype), ref_k.reshape(-1, case.Dk)[rows])
+    assert np.all(mr >= np.abs(vr) * (1 - 1e-15))

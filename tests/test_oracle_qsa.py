@@ -284,3 +284,20 @@ def test_robust_check_accepts_float32_and_rejects_truncation(layout):
         bad[n, j] = np.where(over, c - 1, c)          # one step toward zero in magnitude
     with pytest.raises(AssertionError, match="away from any rounding boundary"):
         check_robust_qsa(bad, values, "bf16")
+
+
+def test_values_out_matches_the_written_keys():
+    """values_out records, for each key written, the float64 value that
+    encodes to it and a magnitude bound that dominates it."""
+    from attention_prologue_kv_gb300 import workloads as wl
+    from helpers import oracle_qsa_inputs
+    from oracle import encoders as enc
+    case = wl.make_qsa_case("vo", 2, 200, Di=32, Dr=16, kbs=16, seed=78, past_max=100)
+    values = {}
+    bk = np.full((case.N, case.Bcap, case.Di), 0x7FBF, dtype=np.uint16)
+    oracle.ref_qsa_prepare(block_keys=bk, values_out=values, **oracle_qsa_inputs(case))
+    written = {(n, j) for n in range(case.N) for j in range(case.Bcap) if not np.all(bk[n, j] == 0x7FBF)}
+    assert set(values) == written and written
+    for (n, j), (u, b) in values.items():
+        assert np.array_equal(enc.bf16_encode(u), bk[n, j])
+        assert np.all(b >= np.abs(u) * (1 - 1e-12))
