@@ -378,7 +378,7 @@ kvr_status qsa_prepare(const kvr_qsa_args* args, cudaStream_t stream);
  * float32 reciprocal product and is within one code of that value (equal to
  * it unless q * 127 / RowMax lies within 2^-15 of a half-integer). With
  * exact = 1 those near-tie codes are recomputed from the exact rational, so
- * every code equals it; this costs about a quarter more time on bf16 rows,
+ * every code equals it; this costs about a third more time on bf16 rows,
  * where such quotients are common. Inputs are finite. Limits: rows >= 0,
  * Hckv >= 1; the outputs must not overlap the input (KVR_ERR_ALIAS).
  */
