@@ -23,8 +23,9 @@ def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None,
         for n, P in enumerate(case.meta["past"]):
             m = min(past_block_keys.shape[1], P // case.kbs, case.Bcap)
             assert np.array_equal(g_bk[n, :m], r_bk[n, :m])
-    n, exact = compare_cache(g_bk, r_bk, "bf16", case.Di)
-    check_robust_qsa(g_bk, values, "bf16")
+    dt = "f16" if case.raw.dtype == torch.float16 else "bf16"
+    n, exact = compare_cache(g_bk, r_bk, dt, case.Di)
+    check_robust_qsa(g_bk, values, dt)
     if carry:
         assert np.array_equal(g_nr, r_nr, equal_nan=True)
         if case.Dr:
@@ -331,3 +332,13 @@ def test_compiled_shape_unaligned_buffers():
         compare_cache(codes_of(bk), r_bk, "bf16", 128)
         assert np.array_equal(f64(nr), r_nr, equal_nan=True)
         assert np.array_equal(f64(npr), r_npr, equal_nan=True)
+
+
+@pytest.mark.parametrize("params_ready", [False, True])
+def test_f16_full_size(params_ready):
+    """The workload's shape with f16 keys, weight and tables (the output type
+    follows the input), in both forms, with carry outputs."""
+    case = wl.make_qsa_case("qsa_f16", 32, 2048, Di=128, Dr=64, kbs=64, seed=1205, past_max=8192, Bcap=160,
+                            in_dtype="f16")
+    n, _ = check(case, params_ready=params_ready)
+    assert n == case.completed_blocks()
