@@ -69,6 +69,10 @@ def parse_args(argv=None):
     ap.add_argument("--profile-range", action="store_true",
                     help="with --only: launch the K steps back to back inside one cudaProfilerStart/Stop range "
                          "(no per-launch timing), for a profiler's range replay")
+    ap.add_argument("--profile-graph", action="store_true",
+                    help="with --profile-range: capture the K steps as one CUDA graph (replayed once untimed "
+                         "first) and replay it inside the range, as the benchmark runs them; for an "
+                         "application-range replay")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -828,6 +832,19 @@ def run_only(args):
     torch.cuda.synchronize()
     if args.profile_range:
         cudart = torch.cuda.cudart()
+        if args.profile_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(args.steps):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            cudart.cudaProfilerStart()
+            g.replay()
+            torch.cuda.synchronize()
+            cudart.cudaProfilerStop()
+            return {"only": args.only, "launches": args.warmup + 2 * args.steps, "range": args.steps,
+                    "graph": True}
         cudart.cudaProfilerStart()
         for _ in range(args.steps):
             fn()
