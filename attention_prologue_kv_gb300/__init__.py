@@ -8,4 +8,4 @@ calling an entry point without the built library raises.
 """
 from .api import (KvrError, PreparedCall, check_bounded_wait, device_copy,  # noqa: E402,F401
                   dynamic_quant, kv_rmsnorm_rope_cache, prepare_kv_rmsnorm_rope_cache, qsa_prepare,
-                  set_debug_validate)
+                  set_debug_validate, store_after_delay)

@@ -5,7 +5,7 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvr.so")
-ABI_VERSION = 8   # KVR_ABI_VERSION of include/kvr.h these structures mirror
+ABI_VERSION = 9   # KVR_ABI_VERSION of include/kvr.h these structures mirror
 
 # kvr_status
 KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS, KVR_ERR_CUDA, KVR_ERR_INDEX = range(8)
@@ -69,7 +69,7 @@ class DqArgs(ctypes.Structure):
 
 EXPORTS = ("kv_rmsnorm_rope_cache", "kv_rmsnorm_rope_cache_staged", "kv_rmsnorm_rope_cache_staged_static",
            "qsa_prepare", "dynamic_quant", "kvr_device_copy",
-           "kvr_check_bounded_wait", "kvr_set_debug_validate",
+           "kvr_check_bounded_wait", "kvr_store_after_delay", "kvr_set_debug_validate",
            "kvr_status_string", "kvr_abi_version")
 
 _lib = None
@@ -100,6 +100,8 @@ def lib():
     L.dynamic_quant.restype = _int
     L.kvr_check_bounded_wait.argtypes = [_vp, _i64, _i64, _vp]
     L.kvr_check_bounded_wait.restype = _int
+    L.kvr_store_after_delay.argtypes = [_vp, _i64, _i64, _vp]
+    L.kvr_store_after_delay.restype = _int
     L.kvr_set_debug_validate.argtypes = [_int]
     L.kvr_set_debug_validate.restype = None
     L.kvr_device_copy.argtypes = [_vp, _vp, _i64, _vp]

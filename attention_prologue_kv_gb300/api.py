@@ -340,6 +340,18 @@ def check_bounded_wait(dev_status, limit_us, abort_after_us=0, stream=None):
         raise KvrError(st, "kvr_check_bounded_wait")
 
 
+def store_after_delay(dev_word, value, delay_us, stream=None):
+    """Test helper: a kernel (programmatic dependent launch) that lets the
+    next launch on `stream` start at once, waits `delay_us` microseconds and
+    then writes `value` into `dev_word` (int64, device, one element): a late
+    producer of an input such as key_length. Asynchronous."""
+    if dev_word.dtype != torch.int64 or dev_word.numel() < 1 or not dev_word.is_cuda:
+        raise ValueError("dev_word must be a CUDA int64 tensor with at least one element")
+    st = N.lib().kvr_store_after_delay(dev_word.data_ptr(), int(value), int(delay_us * 1000), _stream(stream))
+    if st != N.KVR_OK:
+        raise KvrError(st, "kvr_store_after_delay")
+
+
 def dynamic_quant(q_nope, q_out, dequant_scale, *, exact=False, stream=None):
     """DynamicQuant of q^N: per row (last axis, e.g. q^N [T, N, Hckv] gives
     T*N rows) dequant_scale = RowMax(|q|)/127 and q_out = round(q/scale) as

@@ -4,6 +4,9 @@
 // time limit passes or when another warp raises the abort flag. The kernel
 // then records KVR_DEVERR_TIMEOUT and returns, leaving the context usable.
 // No copy is in flight, so the CTA may exit with the phase pending.
+//
+// Also here: a late producer of a device word, for checking that a kernel
+// reads its inputs only after its dependency wait.
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -45,6 +48,22 @@ __global__ void __launch_bounds__(64) bounded_wait_kernel(int32_t* status, uint6
 cudaError_t launch_bounded_wait(int32_t* status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t s) {
     bounded_wait_kernel<<<1, 64, 0, s>>>(status, uint64_t(limit_ns), uint64_t(abort_after_ns));
     return cudaGetLastError();
+}
+
+// One thread: waits for its own predecessor, lets the next launch start at
+// once, spins (bounded by delay_ns) and only then writes *dst, so the
+// dependent grid runs its pre-wait code while the old value is still there.
+__global__ void __launch_bounds__(32) store_after_delay_kernel(int64_t* dst, int64_t value, uint64_t delay_ns) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (threadIdx.x != 0) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < delay_ns) __nanosleep(256);
+    *dst = value;
+}
+
+cudaError_t launch_store_after_delay(int64_t* dst, int64_t value, int64_t delay_ns, cudaStream_t s) {
+    return launch_pdl(store_after_delay_kernel, dim3(1), dim3(32), 0, s, dst, value, uint64_t(delay_ns));
 }
 
 }  // namespace kvr

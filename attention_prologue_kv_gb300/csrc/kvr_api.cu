@@ -53,6 +53,7 @@ cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaSt
 
 // Defined in bounded_wait.cu.
 cudaError_t launch_bounded_wait(int32_t* status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t s);
+cudaError_t launch_store_after_delay(int64_t* dst, int64_t value, int64_t delay_ns, cudaStream_t s);
 // Defined in staging.cu.
 cudaError_t launch_stage_in(void* dst, const void* src, int64_t bytes, cudaStream_t s);
 cudaError_t launch_status_out(int32_t* host_status, const int32_t* dev_status, cudaStream_t s);
@@ -502,6 +503,13 @@ kvr_status kvr_check_bounded_wait(int32_t* dev_status, int64_t limit_ns, int64_t
         return KVR_ERR_SHAPE;
     (void)cudaGetLastError();
     return cuda_status(launch_bounded_wait(dev_status, limit_ns, abort_after_ns, stream));
+}
+
+kvr_status kvr_store_after_delay(int64_t* dev_word, int64_t value, int64_t delay_ns, cudaStream_t stream) {
+    if (dev_word == nullptr) return KVR_ERR_NULL;
+    if (!aligned(dev_word, 8) || delay_ns < 0 || delay_ns > 100000000) return KVR_ERR_SHAPE;
+    (void)cudaGetLastError();
+    return cuda_status(launch_store_after_delay(dev_word, value, delay_ns, stream));
 }
 
 kvr_status dynamic_quant(const kvr_dq_args* a, cudaStream_t stream) {

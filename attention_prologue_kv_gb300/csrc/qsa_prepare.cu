@@ -500,6 +500,19 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
 // lanes of group 0 as 16-byte stores. Needs Di % 8 == 0, Dr % 8 == 0 and
 // 16-byte aligned bases (as the bulk variant).
 //
+// Default form: before the dependency wait each block warp reads key_length
+// with a relaxed load as a hint (the preceding grid may still be writing
+// it), derives the block the hint gives it and prefetches exactly that
+// block's rows, carried rows, first-token cos/sin and, once per sequence,
+// k_norm_weight into L2. Issuing the row prefetch only once the hint has
+// arrived, rather than at the warp's start, leaves the DRAM queues to the
+// running call's own loads a little longer: on the 32 x 2048-token workload
+// a call went from 4.6 to 3.4 us. After the wait the warp loads the real
+// key_length together with the hinted block's data, sums the rows, and
+// compares the two key lengths before anything is written; if they differ
+// it starts over from the real one. Every address taken from the hint is
+// bounds-checked, so a stale or torn hint costs time, never correctness.
+//
 // PR (params_ready): the caller promises that the kernel launched just
 // before does not write key_length, the RoPE tables, past_incomplete_rope
 // or k_norm_weight. The warp then reads key_length, derives its block,
@@ -515,19 +528,32 @@ __global__ void __launch_bounds__(QSA_BULK_THREADS) qsa_bulk_kernel(const QsaPar
 // Warps (candidates) per CTA: 4 measured faster than 1, 2 or 8.
 constexpr int QSA_WARP_TASKS = 4;
 
-// Scalars of sequence n: K = key_length, past length P = K - L, first
-// block j0 = floor(P / KBS) and the number nb of blocks completed by the call.
+// Scalars of sequence n: K = key_length, past length P = K - L (-1 when
+// K < L), first block j0 = floor(P / KBS) and the number nb of blocks
+// completed by the call.
 struct QsaSeq {
     int64_t K, P, j0, nb;
 };
 template <int KBS>
-__device__ __forceinline__ QsaSeq qsa_seq(const QsaParams& p, int64_t n) {
+__device__ __forceinline__ QsaSeq qsa_seq_of(const QsaParams& p, int64_t K) {
     QsaSeq q;
-    q.K = p.key_length[p.key_length_per_seq ? n : 0];
-    q.P = q.K - p.L;
+    q.K = K;
+    q.P = K >= p.L ? K - p.L : -1;
     q.j0 = q.P >= 0 ? q.P / KBS : 0;
     q.nb = q.P >= 0 ? q.K / KBS - q.j0 : 0;
     return q;
+}
+template <int KBS>
+__device__ __forceinline__ QsaSeq qsa_seq(const QsaParams& p, int64_t n) {
+    return qsa_seq_of<KBS>(p, p.key_length[p.key_length_per_seq ? n : 0]);
+}
+
+// A relaxed (morally strong) read, for the key_length hint taken before the
+// dependency wait.
+__device__ __forceinline__ int64_t ld_relaxed_s64(const int64_t* ptr) {
+    int64_t v;
+    asm volatile("ld.relaxed.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+    return v;
 }
 
 // The first token's cos/sin for chunk c (when it lies in the rotated
@@ -553,6 +579,126 @@ __device__ __forceinline__ void qsa_chunk_consts(const QsaParams& p, int64_t n, 
     if (p.w != nullptr) wv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.w) + c * 8);
 }
 
+// L2 prefetch of block jl of sequence n for the scalars q (lane 0 only): its
+// new and carried rows and, with ROPE, its first token's cos/sin (or the
+// carried RoPE row). The caller has checked q.P >= 0, jl < q.nb and
+// q.j0 + jl < Bcap, which keeps every address inside the inputs.
+template <int DI, int KBS, bool ROPE>
+__device__ __forceinline__ void qsa_prefetch_block(const QsaParams& p, const QsaSeq& q, int64_t n, int64_t jl,
+                                                   const uint16_t* raw, const uint16_t* past) {
+    const int64_t tok0 = (q.j0 + jl) * KBS;
+    const int n_past = tok0 < q.P ? int(q.P - tok0) : 0;
+    prefetch_l2_bulk(raw + (tok0 + n_past - q.P) * DI, uint32_t(KBS - n_past) * DI * 2);
+    if (n_past > 0) prefetch_l2_bulk(past, uint32_t(n_past) * DI * 2);
+    if (ROPE && p.Dr > 0) {
+        if (tok0 >= q.P) {
+            prefetch_l2(static_cast<const uint16_t*>(p.cos) + (n * p.L + (tok0 - q.P)) * p.Dr);
+            prefetch_l2(static_cast<const uint16_t*>(p.sin) + (n * p.L + (tok0 - q.P)) * p.Dr);
+        } else {
+            prefetch_l2_bulk(static_cast<const uint16_t*>(p.past_rope) + n * 2 * p.Dr, uint32_t(p.Dr) * 4);
+        }
+    }
+}
+
+// Block jl of sequence n from its scalars q: the row sum (RB loads in flight
+// per lane), mean, normalisation, rotation and the 16-byte stores of the key
+// row by the lanes of group 0. LOADC: load the cos/sin and weight chunk here
+// (otherwise cv, sv, wv hold them). With `verify`, q came from a key_length
+// hint: once the rows are summed, q.K is compared with the real key_length
+// Kt, and on a mismatch nothing is written and false is returned.
+template <class IT, int DI, int KBS, int RB, bool LOADC>
+__device__ __forceinline__ bool qsa_warp_block(const QsaParams& p, const QsaSeq& q, int64_t n, int64_t jl,
+                                               const uint16_t* raw, const uint16_t* past, int c, int g, float* u,
+                                               uint4 cv, uint4 sv, uint4 wv, bool verify, int64_t Kt) {
+    constexpr int C = DI / 8;
+    constexpr int G = 32 / C;
+    constexpr int NR = KBS / G;
+    static_assert(NR % RB == 0, "row batches must tile the block");
+    const int64_t P = q.P;
+    const int64_t j = q.j0 + jl;
+    const int64_t tok0 = j * KBS;
+    // Rows r < n_past are carried (past row r: only the first block can hold
+    // them); row r >= n_past is new row (tok0 - P) + r.
+    const int n_past = tok0 < P ? int(P - tok0) : 0;
+    const int64_t off = (tok0 - P) * DI;
+    if (LOADC) qsa_chunk_consts<DI>(p, n, tok0, P, c, cv, sv, wv);
+
+    // ---- block sum ----
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int b = 0; b < NR; b += RB) {
+        uint4 v[RB];
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+            const int r = g + G * (b + k);
+            const uint16_t* src = r < n_past ? past + r * DI : raw + (off + int64_t(r) * DI);
+            v[k] = ld_stream_v4(src + c * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+            acc[0] = __fadd2_rn(acc[0], make_float2(IT::lo(v[k].x), IT::hi(v[k].x)));
+            acc[1] = __fadd2_rn(acc[1], make_float2(IT::lo(v[k].y), IT::hi(v[k].y)));
+            acc[2] = __fadd2_rn(acc[2], make_float2(IT::lo(v[k].z), IT::hi(v[k].z)));
+            acc[3] = __fadd2_rn(acc[3], make_float2(IT::lo(v[k].w), IT::hi(v[k].w)));
+        }
+    }
+    if (verify && Kt != q.K) return false;   // the same value in every lane
+    float m[8] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y, acc[2].x, acc[2].y, acc[3].x, acc[3].y};
+#pragma unroll
+    for (int o = C; o < 32; o <<= 1)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m[k] += __shfl_xor_sync(0xFFFFFFFFu, m[k], o);
+
+    // ---- mean, optional RMS normalisation (every group holds the whole row) ----
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m[k] *= p.inv_kbs;
+        ss = fmaf(m[k], m[k], ss);
+    }
+    if (p.w != nullptr) {
+#pragma unroll
+        for (int o = 1; o < C; o <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        const float rr = rsqrtf(fmaf(ss, p.inv_di, p.eps));
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[2 * k] = m[2 * k] * rr * IT::lo(ww[k]);
+            m[2 * k + 1] = m[2 * k + 1] * rr * IT::hi(ww[k]);
+        }
+    }
+
+    // ---- rotation of the layout's Dr channels, one rounding, write ----
+    const int base = p.rope_first ? 0 : DI - p.Dr;
+    const int i0 = c * 8 - base;               // table lane of the chunk's first channel
+    if (g == 0 && p.Dr > 0) {
+        reinterpret_cast<float4*>(u + c * 8)[0] = make_float4(m[0], m[1], m[2], m[3]);
+        reinterpret_cast<float4*>(u + c * 8)[1] = make_float4(m[4], m[5], m[6], m[7]);
+    }
+    __syncwarp();
+    if (g != 0) return true;
+    if (p.Dr > 0 && unsigned(i0) < unsigned(p.Dr)) {
+        const int h = p.Dr >> 1;
+        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + k;
+            int la, lb;
+            rope_pair_lanes(i, h, p.rope_half, la, lb);
+            const float a = u[base + la];
+            const float bb = u[base + lb];
+            const float cs = (k & 1) ? IT::hi(cw[k >> 1]) : IT::lo(cw[k >> 1]);
+            const float sn = (k & 1) ? IT::hi(sw[k >> 1]) : IT::lo(sw[k >> 1]);
+            m[k] = i < h ? a * cs - bb * sn : bb * cs + a * sn;
+        }
+    }
+    uint16_t* out = static_cast<uint16_t*>(p.block_keys) + (n * p.Bcap + j) * DI;
+    reinterpret_cast<uint4*>(out)[c] =
+        make_uint4(IT::pack(m[0], m[1]), IT::pack(m[2], m[3]), IT::pack(m[4], m[5]), IT::pack(m[6], m[7]));
+    return true;
+}
+
 template <class IT, int DI, int KBS, bool PR>
 __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_warp_kernel(const QsaParams p) {
     static_assert(DI % 8 == 0 && DI / 8 <= 32 && 32 % (DI / 8) == 0, "one row must span a power-of-two number of lanes");
@@ -563,9 +709,9 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
     // Loads in flight per lane: the whole block when it is at most 32 rows
     // per lane and the constants were read before the wait (PR): 3.51 -> 3.34 us
     // per call on the 32 x 2048-token workload; otherwise batches of 16 (the
-    // default form measured slower with 32: 4.63 -> 4.73 us).
+    // default form measured slower with 32: 4.63 -> 4.73 us, and 3.42 -> 4.49
+    // with the hinted block).
     constexpr int RB = (PR && NR <= 32) ? NR : (NR < 16 ? NR : 16);
-    static_assert(NR % RB == 0, "row batches must tile the block");
     __shared__ __align__(16) float u_s[QSA_WARP_TASKS][DI];
 
     const int lane = threadIdx.x & 31;
@@ -580,8 +726,10 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
     const int64_t jl = int64_t(task - n32 * per_seq);
     const uint16_t* raw = static_cast<const uint16_t*>(p.raw) + n * p.L * DI;
     const uint16_t* past = static_cast<const uint16_t*>(p.past_raw) + n * (KBS - 1) * DI;
+    const int64_t* kl = p.key_length + (p.key_length_per_seq ? n : 0);
 
     QsaSeq q = {0, 0, 0, 0};
+    QsaSeq qh = {0, -1, 0, 0};   // default form: scalars from the key_length hint (P < 0: none usable)
     uint4 cv = make_uint4(0, 0, 0, 0), sv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
     if (live) {
         if (PR) q = qsa_seq<KBS>(p, n);
@@ -602,33 +750,48 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
         } else if (PR) {
             if (q.P >= 0 && jl < q.nb && q.j0 + jl < p.Bcap) {
                 // exactly the block's rows, and its constants
-                const int64_t tok0 = (q.j0 + jl) * KBS;
-                const int n_past = tok0 < q.P ? int(q.P - tok0) : 0;
-                if (lane == 0) {
-                    prefetch_l2_bulk(raw + (tok0 + n_past - q.P) * DI, uint32_t(KBS - n_past) * DI * 2);
-                    if (n_past > 0) prefetch_l2_bulk(past, uint32_t(n_past) * DI * 2);
-                }
-                qsa_chunk_consts<DI>(p, n, tok0, q.P, c, cv, sv, wv);
+                if (lane == 0) qsa_prefetch_block<DI, KBS, false>(p, q, n, jl, raw, past);
+                qsa_chunk_consts<DI>(p, n, (q.j0 + jl) * KBS, q.P, c, cv, sv, wv);
             }
-        } else if (lane == 0) {
+        } else if (jl < p.nbmax) {
+            if (lane == 0 && jl == 0 && p.w != nullptr) prefetch_l2_bulk(p.w, DI * 2);
+            const QsaSeq h = qsa_seq_of<KBS>(p, ld_relaxed_s64(kl));
+            if (h.P >= 0 && jl < h.nb && h.j0 + jl < p.Bcap) {
+                if (lane == 0) qsa_prefetch_block<DI, KBS, true>(p, h, n, jl, raw, past);
+                qh = h;
+            } else if (lane == 0) {
 #if KVR_QSA_RAW_PREFETCH
-            // New-key rows [jl*KBS, (jl+1)*KBS): the block this warp computes
-            // starts P mod KBS rows earlier, but the union over the sequence's
-            // warps covers every row a completed block reads.
-            if (jl < p.nbmax) {
+                // no block from the hint: new-key rows [jl*KBS, (jl+1)*KBS)
                 const int64_t r0 = jl * KBS;
                 prefetch_l2_bulk(raw + r0 * DI, uint32_t(min(int64_t(KBS), p.L - r0) * DI * 2));
+#endif
             }
-#endif
-#if KVR_QSA_KL_PREFETCH
-            if (jl == 0) prefetch_l2(p.key_length + (p.key_length_per_seq ? n : 0));
-#endif
+        } else if (p.next_raw != nullptr) {
+            // carry task: the rows after the last completed block, as the hint
+            // places them
+            const QsaSeq h = qsa_seq_of<KBS>(p, ld_relaxed_s64(kl));
+            if (lane == 0 && h.P >= 0 && h.nb <= p.nbmax) {
+                const int64_t Fn = (h.j0 + h.nb) * KBS;
+                const int64_t rem = h.K - Fn;
+                if (Fn >= h.P && rem > 0 && rem < KBS)
+                    prefetch_l2_bulk(raw + (Fn - h.P) * DI, uint32_t(rem) * DI * 2);
+            }
         }
     }
     pdl_wait();
     pdl_launch_dependents();
     if (!live) return;
-    if (!PR) q = qsa_seq<KBS>(p, n);
+    if (!PR) {
+        if (qh.P >= 0) {
+            // the hinted block's loads go out together with the real key_length
+            const int64_t Kt = *kl;
+            if (qsa_warp_block<IT, DI, KBS, RB, true>(p, qh, n, jl, raw, past, c, g, u_s[wid], cv, sv, wv, true, Kt))
+                return;
+            q = qsa_seq_of<KBS>(p, Kt);   // a stale hint: start over from the real key_length
+        } else {
+            q = qsa_seq<KBS>(p, n);
+        }
+    }
 
     const int64_t P = q.P;
     if (P < 0) {
@@ -677,91 +840,11 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
         return;
     }
     if (jl >= q.nb) return;
-    const int64_t j = q.j0 + jl;
-    if (j >= p.Bcap) {
+    if (q.j0 + jl >= p.Bcap) {
         if (lane == 0 && p.status != nullptr) atomicOr(p.status, KVR_DEVERR_BLOCK_CAP);
         return;
     }
-    const int64_t tok0 = j * KBS;
-    // Rows r < n_past are carried (past row r: only the first block can hold
-    // them); row r >= n_past is new row (tok0 - P) + r.
-    const int n_past = tok0 < P ? int(P - tok0) : 0;
-    const int64_t off = (tok0 - P) * DI;
-    if (!PR) qsa_chunk_consts<DI>(p, n, tok0, P, c, cv, sv, wv);
-
-    // ---- block sum ----
-    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-    for (int b = 0; b < NR; b += RB) {
-        uint4 v[RB];
-#pragma unroll
-        for (int k = 0; k < RB; ++k) {
-            const int r = g + G * (b + k);
-            const uint16_t* src = r < n_past ? past + r * DI : raw + (off + int64_t(r) * DI);
-            v[k] = ld_stream_v4(src + c * 8);
-        }
-#pragma unroll
-        for (int k = 0; k < RB; ++k) {
-            acc[0] = __fadd2_rn(acc[0], make_float2(IT::lo(v[k].x), IT::hi(v[k].x)));
-            acc[1] = __fadd2_rn(acc[1], make_float2(IT::lo(v[k].y), IT::hi(v[k].y)));
-            acc[2] = __fadd2_rn(acc[2], make_float2(IT::lo(v[k].z), IT::hi(v[k].z)));
-            acc[3] = __fadd2_rn(acc[3], make_float2(IT::lo(v[k].w), IT::hi(v[k].w)));
-        }
-    }
-    float m[8] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y, acc[2].x, acc[2].y, acc[3].x, acc[3].y};
-#pragma unroll
-    for (int o = C; o < 32; o <<= 1)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m[k] += __shfl_xor_sync(0xFFFFFFFFu, m[k], o);
-
-    // ---- mean, optional RMS normalisation (every group holds the whole row) ----
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        m[k] *= p.inv_kbs;
-        ss = fmaf(m[k], m[k], ss);
-    }
-    if (p.w != nullptr) {
-#pragma unroll
-        for (int o = 1; o < C; o <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-        const float rr = rsqrtf(fmaf(ss, p.inv_di, p.eps));
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            m[2 * k] = m[2 * k] * rr * IT::lo(ww[k]);
-            m[2 * k + 1] = m[2 * k + 1] * rr * IT::hi(ww[k]);
-        }
-    }
-
-    // ---- rotation of the layout's Dr channels, one rounding, write ----
-    const int base = p.rope_first ? 0 : DI - p.Dr;
-    const int i0 = c * 8 - base;               // table lane of the chunk's first channel
-    float* u = u_s[wid];
-    if (g == 0 && p.Dr > 0) {
-        reinterpret_cast<float4*>(u + c * 8)[0] = make_float4(m[0], m[1], m[2], m[3]);
-        reinterpret_cast<float4*>(u + c * 8)[1] = make_float4(m[4], m[5], m[6], m[7]);
-    }
-    __syncwarp();
-    if (g != 0) return;
-    if (p.Dr > 0 && unsigned(i0) < unsigned(p.Dr)) {
-        const int h = p.Dr >> 1;
-        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = i0 + k;
-            int la, lb;
-            rope_pair_lanes(i, h, p.rope_half, la, lb);
-            const float a = u[base + la];
-            const float bb = u[base + lb];
-            const float cs = (k & 1) ? IT::hi(cw[k >> 1]) : IT::lo(cw[k >> 1]);
-            const float sn = (k & 1) ? IT::hi(sw[k >> 1]) : IT::lo(sw[k >> 1]);
-            m[k] = i < h ? a * cs - bb * sn : bb * cs + a * sn;
-        }
-    }
-    uint16_t* out = static_cast<uint16_t*>(p.block_keys) + (n * p.Bcap + j) * DI;
-    reinterpret_cast<uint4*>(out)[c] =
-        make_uint4(IT::pack(m[0], m[1]), IT::pack(m[2], m[3]), IT::pack(m[4], m[5]), IT::pack(m[6], m[7]));
+    qsa_warp_block<IT, DI, KBS, RB, !PR>(p, q, n, jl, raw, past, c, g, u_s[wid], cv, sv, wv, false, 0);
 }
 
 typedef void (*QsaKernel)(const QsaParams);

@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.kvr_abi_version() == N.ABI_VERSION == 8
+    assert lib.kvr_abi_version() == N.ABI_VERSION == 9
 
 
 def test_status_strings(lib):
@@ -248,6 +248,13 @@ def test_python_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         kvr.kv_rmsnorm_rope_cache(x, x[0, 0, 0, :512], x, x, torch.zeros(6, dtype=torch.int64),
                                   x, x)
+
+
+def test_store_after_delay_validation(lib):
+    assert lib.kvr_store_after_delay(None, 5, 1000, None) == N.KVR_ERR_NULL
+    assert lib.kvr_store_after_delay((1 << 20) + 4, 5, 1000, None) == N.KVR_ERR_SHAPE    # not 8-byte aligned
+    assert lib.kvr_store_after_delay(1 << 20, 5, -1, None) == N.KVR_ERR_SHAPE
+    assert lib.kvr_store_after_delay(1 << 20, 5, 10**8 + 1, None) == N.KVR_ERR_SHAPE     # above 0.1 s
 
 
 def test_bounded_wait_check_validation(lib):

@@ -12,11 +12,12 @@ from helpers import check_robust_qsa, compare_cache, run_gpu_qsa, run_oracle_qsa
 pytestmark = pytest.mark.gpu
 
 
-def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None, params_ready=False):
+def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None, params_ready=False,
+          late_key_length=None):
     kw = dict(carry=carry, rope_layout=rope_layout, past_block_keys=past_block_keys)
     values = {}
     r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, values_out=values, **kw)
-    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=params_ready, **kw)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=params_ready, late_key_length=late_key_length, **kw)
     assert g_st == r_st
     if past_block_keys is not None:
         # copied past rows are bit-exact copies
@@ -57,6 +58,24 @@ def test_features_disabled(rope, norm):
 def test_shared_key_length():
     case = wl.make_qsa_case("k", 4, 33, Di=64, Dr=16, kbs=8, seed=8, shared_length=True)
     check(case)
+
+
+@pytest.mark.parametrize("late", ["same", "one_block_more", "ragged_less", "below_L", "huge"])
+@pytest.mark.parametrize("L,Di,kbs", [(2048, 128, 64), (300, 64, 32), (45, 256, 128)])
+def test_key_length_written_late_by_the_preceding_kernel(late, L, Di, kbs):
+    """The default form reads key_length before its dependency wait only as
+    a prefetch hint. Here the kernel launched just before the call lets it
+    start and writes key_length afterwards; the call still finds the blocks,
+    carry outputs and status of the late value, whatever the stale one was:
+    the same, a block further on, a ragged amount less, shorter than L (no
+    usable hint), or huge (blocks beyond Bcap)."""
+    case = wl.make_qsa_case("late", 8, L, Di=Di, Dr=64, kbs=kbs, seed=L + Di + kbs, past_max=4 * kbs + 7,
+                            shared_length=True)
+    K = int(case.key_length[0])
+    old = {"same": K, "one_block_more": K + kbs, "ragged_less": max(K - 17, 0), "below_L": L - 1,
+           "huge": 1 << 62}[late]
+    n, _ = check(case, late_key_length=old)
+    assert n == case.completed_blocks()
 
 
 def test_no_block_completed_only_carry():
