@@ -100,7 +100,7 @@ def lib():
     L.dynamic_quant.restype = _int
     L.kvr_check_bounded_wait.argtypes = [_vp, _i64, _i64, _vp]
     L.kvr_check_bounded_wait.restype = _int
-    L.kvr_store_after_delay.argtypes = [_vp, _i64, _i64, _vp]
+    L.kvr_store_after_delay.argtypes = [_vp, _vp, _i64, _i64, _vp]
     L.kvr_store_after_delay.restype = _int
     L.kvr_set_debug_validate.argtypes = [_int]
     L.kvr_set_debug_validate.restype = None

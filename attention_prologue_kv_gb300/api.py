@@ -340,14 +340,19 @@ def check_bounded_wait(dev_status, limit_us, abort_after_us=0, stream=None):
         raise KvrError(st, "kvr_check_bounded_wait")
 
 
-def store_after_delay(dev_word, value, delay_us, stream=None):
+def store_after_delay(dst, src, delay_us, stream=None):
     """Test helper: a kernel (programmatic dependent launch) that lets the
     next launch on `stream` start at once, waits `delay_us` microseconds and
-    then writes `value` into `dev_word` (int64, device, one element): a late
-    producer of an input such as key_length. Asynchronous."""
-    if dev_word.dtype != torch.int64 or dev_word.numel() < 1 or not dev_word.is_cuda:
-        raise ValueError("dev_word must be a CUDA int64 tensor with at least one element")
-    st = N.lib().kvr_store_after_delay(dev_word.data_ptr(), int(value), int(delay_us * 1000), _stream(stream))
+    then copies `src` into `dst` (contiguous int64 CUDA tensors of the same
+    size): a late producer of an input such as key_length. Asynchronous; keep
+    both tensors alive until the stream has passed it."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if t.dtype != torch.int64 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA int64 tensor" % name)
+    if dst.numel() != src.numel():
+        raise ValueError("dst and src must have the same number of elements")
+    st = N.lib().kvr_store_after_delay(dst.data_ptr(), src.data_ptr(), dst.numel(), int(delay_us * 1000),
+                                       _stream(stream))
     if st != N.KVR_OK:
         raise KvrError(st, "kvr_store_after_delay")
 

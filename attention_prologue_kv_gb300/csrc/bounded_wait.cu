@@ -50,20 +50,22 @@ cudaError_t launch_bounded_wait(int32_t* status, int64_t limit_ns, int64_t abort
     return cudaGetLastError();
 }
 
-// One thread: waits for its own predecessor, lets the next launch start at
-// once, spins (bounded by delay_ns) and only then writes *dst, so the
-// dependent grid runs its pre-wait code while the old value is still there.
-__global__ void __launch_bounds__(32) store_after_delay_kernel(int64_t* dst, int64_t value, uint64_t delay_ns) {
+// One warp: waits for its own predecessor, lets the next launch start at
+// once, spins (bounded by delay_ns) and only then copies src[0..count) to
+// dst, so the dependent grid runs its pre-wait code while the old values are
+// still there.
+__global__ void __launch_bounds__(32) store_after_delay_kernel(int64_t* dst, const int64_t* src, int64_t count,
+                                                               uint64_t delay_ns) {
     pdl_wait();
     pdl_launch_dependents();
-    if (threadIdx.x != 0) return;
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < delay_ns) __nanosleep(256);
-    *dst = value;
+    for (int64_t i = threadIdx.x; i < count; i += 32) dst[i] = src[i];
 }
 
-cudaError_t launch_store_after_delay(int64_t* dst, int64_t value, int64_t delay_ns, cudaStream_t s) {
-    return launch_pdl(store_after_delay_kernel, dim3(1), dim3(32), 0, s, dst, value, uint64_t(delay_ns));
+cudaError_t launch_store_after_delay(int64_t* dst, const int64_t* src, int64_t count, int64_t delay_ns,
+                                     cudaStream_t s) {
+    return launch_pdl(store_after_delay_kernel, dim3(1), dim3(32), 0, s, dst, src, count, uint64_t(delay_ns));
 }
 
 }  // namespace kvr

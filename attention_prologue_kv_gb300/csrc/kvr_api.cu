@@ -53,7 +53,8 @@ cudaError_t launch_device_copy(void* dst, const void* src, int64_t bytes, cudaSt
 
 // Defined in bounded_wait.cu.
 cudaError_t launch_bounded_wait(int32_t* status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t s);
-cudaError_t launch_store_after_delay(int64_t* dst, int64_t value, int64_t delay_ns, cudaStream_t s);
+cudaError_t launch_store_after_delay(int64_t* dst, const int64_t* src, int64_t count, int64_t delay_ns,
+                                     cudaStream_t s);
 // Defined in staging.cu.
 cudaError_t launch_stage_in(void* dst, const void* src, int64_t bytes, cudaStream_t s);
 cudaError_t launch_status_out(int32_t* host_status, const int32_t* dev_status, cudaStream_t s);
@@ -505,11 +506,15 @@ kvr_status kvr_check_bounded_wait(int32_t* dev_status, int64_t limit_ns, int64_t
     return cuda_status(launch_bounded_wait(dev_status, limit_ns, abort_after_ns, stream));
 }
 
-kvr_status kvr_store_after_delay(int64_t* dev_word, int64_t value, int64_t delay_ns, cudaStream_t stream) {
-    if (dev_word == nullptr) return KVR_ERR_NULL;
-    if (!aligned(dev_word, 8) || delay_ns < 0 || delay_ns > 100000000) return KVR_ERR_SHAPE;
+kvr_status kvr_store_after_delay(int64_t* dst, const int64_t* src, int64_t count, int64_t delay_ns,
+                                 cudaStream_t stream) {
+    if (count < 0 || count > (int64_t(1) << 20) || delay_ns < 0 || delay_ns > 100000000) return KVR_ERR_SHAPE;
+    if (count == 0) return KVR_OK;
+    if (dst == nullptr || src == nullptr) return KVR_ERR_NULL;
+    if (!aligned(dst, 8) || !aligned(src, 8)) return KVR_ERR_SHAPE;
+    if (overlap(dst, count * 8, src, count * 8)) return KVR_ERR_ALIAS;
     (void)cudaGetLastError();
-    return cuda_status(launch_store_after_delay(dev_word, value, delay_ns, stream));
+    return cuda_status(launch_store_after_delay(dst, src, count, delay_ns, stream));
 }
 
 kvr_status dynamic_quant(const kvr_dq_args* a, cudaStream_t stream) {

@@ -410,18 +410,22 @@ kvr_status kvr_device_copy(void* dst, const void* src, int64_t bytes, cudaStream
  * usable. Asynchronous on `stream`. */
 kvr_status kvr_check_bounded_wait(int32_t* dev_status, int64_t limit_ns, int64_t abort_after_ns, cudaStream_t stream);
 
-/* Test helper (no counterpart on the pages): a late producer of a device
- * word. One small kernel, launched with programmatic dependent launch like
+/* Test helper (no counterpart on the pages): a late producer of device
+ * words. One small kernel, launched with programmatic dependent launch like
  * the calls above, waits for its own predecessor on `stream`, lets the next
  * launch on `stream` start at once, spins for `delay_ns` nanoseconds
- * (0 .. 1e8) and only then writes `value` to the 8-byte-aligned device word
- * *dev_word. A call launched right after it therefore starts while the word
- * still holds its old value, and must see `value` after its dependency wait:
+ * (0 .. 1e8) and only then copies `count` (0 .. 2^20) int64 words from the
+ * device array `src` to the device array `dst` (both 8-byte aligned, not
+ * overlapping; the caller keeps both alive until the stream has passed the
+ * kernel). A call launched right after it therefore starts while `dst` still
+ * holds its old values, and must see the new ones after its dependency wait:
  * the check that qsa_prepare's default form takes key_length only after the
- * wait (its earlier read is a prefetch hint). Returns KVR_ERR_NULL for a null
- * pointer, KVR_ERR_SHAPE for a misaligned one or a delay out of range.
- * Asynchronous on `stream`. */
-kvr_status kvr_store_after_delay(int64_t* dev_word, int64_t value, int64_t delay_ns, cudaStream_t stream);
+ * wait (its earlier read is a prefetch hint). Returns KVR_ERR_SHAPE for a
+ * count or delay out of range or a misaligned pointer, KVR_ERR_NULL for a
+ * null pointer (count > 0), KVR_ERR_ALIAS for overlapping arrays; count 0
+ * launches nothing. Asynchronous on `stream`. */
+kvr_status kvr_store_after_delay(int64_t* dst, const int64_t* src, int64_t count, int64_t delay_ns,
+                                 cudaStream_t stream);
 
 /* Debug validation of kv_rmsnorm_rope_cache's index (off by default; the
  * environment variable KVR_DEBUG_VALIDATE=1 turns it on at the first call,

@@ -277,10 +277,11 @@ def compare_cache(gpu, ref, dtype, D):
 def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="interleave_last",
                 past_block_keys=None, params_ready=False, late_key_length=None):
     """past_block_keys: codes [N, Bp, Di] (numpy) for the concat-output form.
-    late_key_length: the device key_length (one shared entry) starts out
-    holding this value, and a kernel launched just before the call, which
-    lets the call start at once, writes the case's key_length only after a
-    delay (kvr.store_after_delay): the call must use the late value."""
+    late_key_length: the device key_length starts out holding these values
+    (int64 tensor shaped like case.key_length), and a kernel launched just
+    before the call, which lets the call start at once, writes the case's
+    key_length only after a delay (kvr.store_after_delay): the call must use
+    the late values."""
     import attention_prologue_kv_gb300 as kvr
     from attention_prologue_kv_gb300.workloads import SENTINEL16
     bk = block_keys
@@ -306,9 +307,9 @@ def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="int
         torch.from_numpy(past_block_keys.view(np.int16)).to(dev).view(case.raw.dtype)
     if late_key_length is not None:
         kl = ins[1]
-        assert kl.numel() == 1, "the late store writes one shared key_length"
-        kl.fill_(int(late_key_length))
-        kvr.store_after_delay(kl, int(case.key_length[0]), delay_us=200)
+        true_kl = kl.clone()
+        kl.copy_(late_key_length.reshape(kl.shape))
+        kvr.store_after_delay(kl, true_kl, delay_us=200)
     kvr.qsa_prepare(ins[0], bk, ins[1], ins[2], ins[3], ins[4], ins[5], ins[6], case.kbs, case.eps,
                     next_incomplete_raw_keys=nr, next_incomplete_rope=npr, dev_status=status,
                     rope_layout=rope_layout, past_block_index_keys=pbk, params_ready=params_ready)

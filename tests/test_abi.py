@@ -251,10 +251,16 @@ def test_python_binding_rejects_cpu_tensors():
 
 
 def test_store_after_delay_validation(lib):
-    assert lib.kvr_store_after_delay(None, 5, 1000, None) == N.KVR_ERR_NULL
-    assert lib.kvr_store_after_delay((1 << 20) + 4, 5, 1000, None) == N.KVR_ERR_SHAPE    # not 8-byte aligned
-    assert lib.kvr_store_after_delay(1 << 20, 5, -1, None) == N.KVR_ERR_SHAPE
-    assert lib.kvr_store_after_delay(1 << 20, 5, 10**8 + 1, None) == N.KVR_ERR_SHAPE     # above 0.1 s
+    d, s = 1 << 20, 1 << 21
+    assert lib.kvr_store_after_delay(None, s, 4, 1000, None) == N.KVR_ERR_NULL
+    assert lib.kvr_store_after_delay(d, None, 4, 1000, None) == N.KVR_ERR_NULL
+    assert lib.kvr_store_after_delay(d + 4, s, 4, 1000, None) == N.KVR_ERR_SHAPE       # not 8-byte aligned
+    assert lib.kvr_store_after_delay(d, s, -1, 1000, None) == N.KVR_ERR_SHAPE
+    assert lib.kvr_store_after_delay(d, s, (1 << 20) + 1, 1000, None) == N.KVR_ERR_SHAPE
+    assert lib.kvr_store_after_delay(d, s, 4, -1, None) == N.KVR_ERR_SHAPE
+    assert lib.kvr_store_after_delay(d, s, 4, 10**8 + 1, None) == N.KVR_ERR_SHAPE      # above 0.1 s
+    assert lib.kvr_store_after_delay(d, d + 8, 4, 1000, None) == N.KVR_ERR_ALIAS       # overlapping
+    assert lib.kvr_store_after_delay(None, None, 0, 1000, None) == N.KVR_OK             # nothing to copy
 
 
 def test_bounded_wait_check_validation(lib):

@@ -60,22 +60,36 @@ def test_shared_key_length():
     check(case)
 
 
-@pytest.mark.parametrize("late", ["same", "one_block_more", "ragged_less", "below_L", "huge"])
-@pytest.mark.parametrize("L,Di,kbs", [(2048, 128, 64), (300, 64, 32), (45, 256, 128)])
-def test_key_length_written_late_by_the_preceding_kernel(late, L, Di, kbs):
+def stale_key_lengths(case, late):
+    K = case.key_length
+    return {"same": K.clone(), "one_block_more": K + case.kbs, "ragged_less": (K - 17).clamp(min=0),
+            "below_L": torch.full_like(K, case.L - 1), "huge": torch.full_like(K, 1 << 62),
+            "mixed": torch.where(torch.arange(K.numel()) % 2 == 0, K + 3, K)}[late]
+
+
+@pytest.mark.parametrize("late", ["same", "one_block_more", "ragged_less", "below_L", "huge", "mixed"])
+@pytest.mark.parametrize("L,Di,kbs,shared", [(2048, 128, 64, False), (300, 64, 32, True), (45, 256, 128, False)])
+def test_key_length_written_late_by_the_preceding_kernel(late, L, Di, kbs, shared):
     """The default form reads key_length before its dependency wait only as
     a prefetch hint. Here the kernel launched just before the call lets it
     start and writes key_length afterwards; the call still finds the blocks,
-    carry outputs and status of the late value, whatever the stale one was:
-    the same, a block further on, a ragged amount less, shorter than L (no
-    usable hint), or huge (blocks beyond Bcap)."""
+    carry outputs and status of the late values, whatever the stale ones
+    were: the same, a block further on, a ragged amount less, shorter than L
+    (no usable hint), huge (blocks beyond Bcap), or stale in every other
+    sequence only."""
     case = wl.make_qsa_case("late", 8, L, Di=Di, Dr=64, kbs=kbs, seed=L + Di + kbs, past_max=4 * kbs + 7,
-                            shared_length=True)
-    K = int(case.key_length[0])
-    old = {"same": K, "one_block_more": K + kbs, "ragged_less": max(K - 17, 0), "below_L": L - 1,
-           "huge": 1 << 62}[late]
-    n, _ = check(case, late_key_length=old)
+                            shared_length=shared)
+    n, _ = check(case, late_key_length=stale_key_lengths(case, late))
     assert n == case.completed_blocks()
+
+
+@pytest.mark.parametrize("late", ["one_block_more", "mixed"])
+def test_key_length_written_late_full_size(late):
+    """The benchmark's workload (32 sequences of 2048 new tokens, per-sequence
+    key_length) with its key lengths written after the call has started."""
+    case = wl.qsa_prepare_workload()
+    n, _ = check(case, late_key_length=stale_key_lengths(case, late))
+    assert n == case.completed_blocks() == 1024
 
 
 def test_no_block_completed_only_carry():
