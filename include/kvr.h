@@ -48,9 +48,11 @@
  *     its copies in flight land, and returns.
  *   - Each launch uses programmatic dependent launch: it may start while the
  *     previous kernel on the stream finishes, and waits for that kernel's
- *     results before it reads any input (the one exception is opt-in:
- *     kvr_kv_args.params_ready lets gamma and the scales be read earlier).
- *     Before the wait a kernel only issues L2 prefetches of its inputs.
+ *     results before it uses any input (the one exception is opt-in:
+ *     the params_ready flags let constants be read earlier). Before the wait
+ *     a kernel issues L2 prefetches of its inputs; qsa_prepare's
+ *     compiled-shape kernel also reads key_length there, as a hint for those
+ *     prefetches only (a relaxed read), and takes its value after the wait.
  *   - An empty problem (T = Bkv*Skv = 0, or N = 0) returns KVR_OK with no
  *     launch, mirroring the empty-tensor rule of "aclnnMlaPrologV3WeightNz"
  *     ("Shape restrictions": caches are not updated). A qsa_prepare call
@@ -313,9 +315,13 @@ typedef enum kvr_qsa_rope {
  *                   KVR_DEVERR_PAST_BLOCKS, the missing rows stay untouched),
  *                   so block_keys ends as the past keys followed by the new
  *                   ones. It must not overlap block_keys or the next_* outputs.
- *   params_ready    0 (default): every input is read after the kernel waits
- *                   for the preceding kernel on the stream (programmatic
- *                   dependent launch). Nonzero: the caller promises that the
+ *   params_ready    0 (default): every input is used as read after the kernel
+ *                   waits for the preceding kernel on the stream (programmatic
+ *                   dependent launch); the compiled-shape kernel reads
+ *                   key_length once before that wait as a prefetch hint and
+ *                   compares it with the value read after it (a stale hint,
+ *                   e.g. key_length written by that preceding kernel, costs
+ *                   time, never correctness). Nonzero: the caller promises that the
  *                   kernel launched immediately before this call on `stream`
  *                   writes none of key_length, rope_cos, rope_sin,
  *                   past_incomplete_rope and k_norm_weight (true when
