@@ -47,8 +47,12 @@ constexpr int BULK_THREADS = 32 * (1 + BULK_CONSUMERS);
 #ifndef KVR_BULK_CTAS_PER_SM
 #define KVR_BULK_CTAS_PER_SM 1
 #endif
-// Before the dependency wait, prefetch this CTA's first KVR_BULK_PREFETCH
-// ring-fulls of tiles into L2 (a hint only: L2 is the coherence point).
+// Before the dependency wait, prefetch this CTA's first S - 1 tiles (all but
+// one stage of its ring) into L2; a hint only, L2 is the coherence point.
+// The next call's CTAs start as this call's CTAs finish, and their prefetch
+// burst shares DRAM with this call's tail: on the 32768-token prefill (S = 4
+// stages of 32 rows) a call took 15.4 us with no prefetch, 14.75 / 14.1 /
+// 14.05 us with 1 / 2 / 3 tiles and 14.55 us with the whole ring.
 #ifndef KVR_BULK_PREFETCH
 #define KVR_BULK_PREFETCH 1
 #endif
@@ -87,7 +91,8 @@ __global__ void __launch_bounds__(BULK_THREADS, KVR_BULK_CTAS_PER_SM) kv_bulk_ke
         fence_mbar_init();
 #if KVR_BULK_PREFETCH
         int64_t it = 0;
-        for (int64_t r0 = lo; r0 < hi && it < int64_t(KVR_BULK_PREFETCH) * p.S; r0 += p.R, ++it) {
+        const int64_t npf = p.S > 1 ? p.S - 1 : 1;
+        for (int64_t r0 = lo; r0 < hi && it < npf; r0 += p.R, ++it) {
             const int rows = int(hi - r0 < p.R ? hi - r0 : p.R);
             if (p.kv_contig) prefetch_l2_bulk(static_cast<const char*>(p.kv) + r0 * kv_row, rows * kv_row);
             prefetch_l2_bulk(static_cast<const char*>(p.cos) + r0 * cs_row, rows * cs_row);
