@@ -587,10 +587,10 @@ def hold_stream(ms=1.0):
     torch.cuda._sleep(int(ms * 2e6))   # cycles at ~2 GHz
 
 
-def time_graph(calls, n_calls, stream):
+def time_graph(calls, n_calls, stream, reps=3):
     """Average duration of one call when n_calls calls (cycling through
     `calls`) run back to back as one CUDA graph replay (after one untimed
-    replay)."""
+    replay); the median over `reps` timed replays."""
     import torch
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -598,14 +598,17 @@ def time_graph(calls, n_calls, stream):
             calls[i % len(calls)]()
     g.replay()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    hold_stream()
-    e0.record(stream)
-    g.replay()
-    e1.record(stream)
-    e1.synchronize()
-    return e0.elapsed_time(e1) / n_calls
+    ts = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        hold_stream()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / n_calls)
+    return statistics.median(ts)
 
 
 def run_extras(dev, kvr, flush_buf, peak):
