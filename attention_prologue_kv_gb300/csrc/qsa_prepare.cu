@@ -709,8 +709,8 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
     // Loads in flight per lane: the whole block when it is at most 32 rows
     // per lane and the constants were read before the wait (PR): 3.51 -> 3.34 us
     // per call on the 32 x 2048-token workload; otherwise batches of 16 (the
-    // default form measured slower with 32: 4.63 -> 4.73 us, and 3.42 -> 4.49
-    // with the hinted block).
+    // default form measured slower with 32: 4.63 -> 4.73 us with the window
+    // prefetch, 3.58 -> 4.59 us with the hinted block).
     constexpr int RB = (PR && NR <= 32) ? NR : (NR < 16 ? NR : 16);
     __shared__ __align__(16) float u_s[QSA_WARP_TASKS][DI];
 
