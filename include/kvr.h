@@ -321,7 +321,9 @@ typedef enum kvr_qsa_rope {
  *                   key_length once before that wait as a prefetch hint and
  *                   compares it with the value read after it (a stale hint,
  *                   e.g. key_length written by that preceding kernel, costs
- *                   time, never correctness). Nonzero: the caller promises that the
+ *                   time, never correctness: the warp sums its block a second
+ *                   time, about 2 us on the 32 x 2048-token workload). Nonzero:
+ *                   the caller promises that the
  *                   kernel launched immediately before this call on `stream`
  *                   writes none of key_length, rope_cos, rope_sin,
  *                   past_incomplete_rope and k_norm_weight (true when
