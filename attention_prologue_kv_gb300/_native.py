@@ -5,7 +5,7 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvr.so")
-ABI_VERSION = 9   # KVR_ABI_VERSION of include/kvr.h these structures mirror
+ABI_VERSION = 10   # KVR_ABI_VERSION of include/kvr.h these structures mirror
 
 # kvr_status
 KVR_OK, KVR_ERR_NULL, KVR_ERR_SHAPE, KVR_ERR_DTYPE, KVR_ERR_MODE, KVR_ERR_ALIAS, KVR_ERR_CUDA, KVR_ERR_INDEX = range(8)
@@ -55,7 +55,7 @@ class QsaArgs(ctypes.Structure):
         ("next_incomplete_raw_keys", _vp), ("next_incomplete_rope", _vp),
         ("dev_status", _vp),
         ("rope_layout", _int), ("past_block_index_keys", _vp), ("Bp", _i64),
-        ("params_ready", ctypes.c_int32),
+        ("params_ready", ctypes.c_int32), ("key_length_late", ctypes.c_int32),
     ]
 
 

@@ -236,7 +236,8 @@ def prepare_kv_rmsnorm_rope_cache(kv, gamma, cos, sin, index, ckv_cache, k_cache
 def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_norm_weight,
                 past_incomplete_raw_keys, past_incomplete_rope, key_block_size, epsilon=1e-6, *,
                 next_incomplete_raw_keys=None, next_incomplete_rope=None, dev_status=None,
-                rope_layout="interleave_last", past_block_index_keys=None, params_ready=False, stream=None):
+                rope_layout="interleave_last", past_block_index_keys=None, params_ready=False,
+                key_length_late=False, stream=None):
     """QSA block-key prepare. Positional arguments follow the qsa_prepare
     parameter list; `block_keys` [N, Bcap, Di] holds the past block keys and
     receives the new ones in place (block j at row j). rope_cos/rope_sin
@@ -250,7 +251,11 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
     j < floor(P/kbs) are copied into block_keys first. params_ready=True
     promises that the kernel launched just before this call writes none of
     key_length, rope_cos/rope_sin, past_incomplete_rope and k_norm_weight,
-    so the compiled-shape kernel may read them before its dependency wait."""
+    so the compiled-shape kernel may read them before its dependency wait.
+    Without it, that kernel reads key_length before the wait only as a
+    prefetch hint; key_length_late=True says the kernel launched just before
+    writes key_length, and skips the hint (same results, no second pass when
+    the hint would be stale)."""
     raw = _cuda(raw_index_keys, "raw_index_keys")
     if raw.dim() != 3:
         raise ValueError("raw_index_keys must be [N, L, Di]")
@@ -309,7 +314,7 @@ def qsa_prepare(raw_index_keys, block_keys, key_length, rope_cos, rope_sin, k_no
         next_incomplete_rope=_ptr(next_incomplete_rope, "next_incomplete_rope"),
         dev_status=_ptr(dev_status, "dev_status"), rope_layout=N.QSA_ROPE_LAYOUTS[rope_layout],
         past_block_index_keys=_past_ptr(past_block_index_keys, raw.device), Bp=Bp,
-        params_ready=1 if params_ready else 0)
+        params_ready=1 if params_ready else 0, key_length_late=1 if key_length_late else 0)
     if block_keys.shape[0] != Nn or block_keys.shape[2] != Di:
         raise ValueError("block_keys must be [N, Bcap, Di]")
     st = N.lib().qsa_prepare(ctypes.byref(a), _stream(stream))

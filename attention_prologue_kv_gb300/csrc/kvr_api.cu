@@ -489,6 +489,7 @@ kvr_status qsa_prepare(const kvr_qsa_args* a, cudaStream_t stream) {
     p.rope_first = a->rope_layout == KVR_QSA_ROPE_INTERLEAVE_FIRST || a->rope_layout == KVR_QSA_ROPE_HALF_FIRST;
     p.rope_half = a->rope_layout == KVR_QSA_ROPE_HALF_LAST || a->rope_layout == KVR_QSA_ROPE_HALF_FIRST;
     p.params_ready = a->params_ready != 0;
+    p.key_length_late = a->key_length_late != 0;
     p.eps = a->eps;
     p.inv_di = 1.0f / float(a->Di);
     p.inv_kbs = 1.0f / float(kbs);

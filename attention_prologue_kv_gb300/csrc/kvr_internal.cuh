@@ -275,6 +275,7 @@ struct QsaParams {
     int rope_first;      // rotate channels [0, Dr) instead of [Di-Dr, Di)
     int rope_half;       // rotate-half pairs (x[i], x[i+Dr/2]) instead of (x[2i], x[2i+1])
     int params_ready;    // key_length, tables and weight may be read before the dependency wait
+    int key_length_late; // no early key_length hint (the preceding kernel writes it)
     float eps, inv_di, inv_kbs;
 };
 

@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
             }
         } else if (jl < p.nbmax) {
             if (lane == 0 && jl == 0 && p.w != nullptr) prefetch_l2_bulk(p.w, DI * 2);
-            const QsaSeq h = qsa_seq_of<KBS>(p, ld_relaxed_s64(kl));
+            const QsaSeq h = p.key_length_late ? QsaSeq{0, -1, 0, 0} : qsa_seq_of<KBS>(p, ld_relaxed_s64(kl));
             if (h.P >= 0 && jl < h.nb && h.j0 + jl < p.Bcap) {
                 if (lane == 0) qsa_prefetch_block<DI, KBS, true>(p, h, n, jl, raw, past);
                 qh = h;
@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(32 * QSA_WARP_TASKS, 16 / QSA_WARP_TASKS) qsa_
                 prefetch_l2_bulk(raw + r0 * DI, uint32_t(min(int64_t(KBS), p.L - r0) * DI * 2));
 #endif
             }
-        } else if (p.next_raw != nullptr) {
+        } else if (p.next_raw != nullptr && !p.key_length_late) {
             // carry task: the rows after the last completed block, as the hint
             // places them
             const QsaSeq h = qsa_seq_of<KBS>(p, ld_relaxed_s64(kl));

@@ -52,7 +52,8 @@
  *     the params_ready flags let constants be read earlier). Before the wait
  *     a kernel issues L2 prefetches of its inputs; qsa_prepare's
  *     compiled-shape kernel also reads key_length there, as a hint for those
- *     prefetches only (a relaxed read), and takes its value after the wait.
+ *     prefetches only (a relaxed read; kvr_qsa_args.key_length_late turns
+ *     it off), and takes its value after the wait.
  *   - An empty problem (T = Bkv*Skv = 0, or N = 0) returns KVR_OK with no
  *     launch, mirroring the empty-tensor rule of "aclnnMlaPrologV3WeightNz"
  *     ("Shape restrictions": caches are not updated). A qsa_prepare call
@@ -75,7 +76,7 @@
 extern "C" {
 #endif
 
-#define KVR_ABI_VERSION 9
+#define KVR_ABI_VERSION 10
 
 typedef enum kvr_status {
     KVR_OK = 0,
@@ -334,6 +335,13 @@ typedef enum kvr_qsa_rope {
  *                   that wait, so that only the key rows are read after it.
  *                   Other shapes ignore the flag. Breaking the promise gives
  *                   stale values.
+ *   key_length_late 0 (default): as above. Nonzero (with params_ready 0): the
+ *                   caller says that the kernel launched immediately before
+ *                   this call writes key_length, so an early read would be
+ *                   stale; the compiled-shape kernel then takes no key_length
+ *                   hint and prefetches each warp's window of new keys
+ *                   instead, which skips the second pass a stale hint costs.
+ *                   Results are the same either way.
  *
  * Limits: N, L >= 0; Di >= 1; 0 <= Dr <= Di, Dr even; Bcap >= 1; Bp >= 0.
  * Mean, normalisation and rotation in float32, one rounding to `in_dtype`.
@@ -361,6 +369,7 @@ typedef struct kvr_qsa_args {
     const void* past_block_index_keys;
     int64_t Bp;
     int32_t params_ready;
+    int32_t key_length_late;
 } kvr_qsa_args;
 
 kvr_status qsa_prepare(const kvr_qsa_args* args, cudaStream_t stream);

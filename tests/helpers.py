@@ -275,7 +275,7 @@ def compare_cache(gpu, ref, dtype, D):
 
 
 def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="interleave_last",
-                past_block_keys=None, params_ready=False, late_key_length=None):
+                past_block_keys=None, params_ready=False, late_key_length=None, key_length_late=False):
     """past_block_keys: codes [N, Bp, Di] (numpy) for the concat-output form.
     late_key_length: the device key_length starts out holding these values
     (int64 tensor shaped like case.key_length), and a kernel launched just
@@ -312,7 +312,8 @@ def run_gpu_qsa(case, carry=False, block_keys=None, dev="cuda", rope_layout="int
         kvr.store_after_delay(kl, true_kl, delay_us=200)
     kvr.qsa_prepare(ins[0], bk, ins[1], ins[2], ins[3], ins[4], ins[5], ins[6], case.kbs, case.eps,
                     next_incomplete_raw_keys=nr, next_incomplete_rope=npr, dev_status=status,
-                    rope_layout=rope_layout, past_block_index_keys=pbk, params_ready=params_ready)
+                    rope_layout=rope_layout, past_block_index_keys=pbk, params_ready=params_ready,
+                    key_length_late=key_length_late)
     torch.cuda.synchronize()
     for c in checks:
         c()

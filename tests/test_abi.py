@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.kvr_abi_version() == N.ABI_VERSION == 9
+    assert lib.kvr_abi_version() == N.ABI_VERSION == 10
 
 
 def test_status_strings(lib):

@@ -13,11 +13,12 @@ pytestmark = pytest.mark.gpu
 
 
 def check(case, carry=True, rope_layout="interleave_last", past_block_keys=None, params_ready=False,
-          late_key_length=None):
+          late_key_length=None, key_length_late=False):
     kw = dict(carry=carry, rope_layout=rope_layout, past_block_keys=past_block_keys)
     values = {}
     r_bk, r_nr, r_npr, r_st = run_oracle_qsa(case, values_out=values, **kw)
-    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=params_ready, late_key_length=late_key_length, **kw)
+    g_bk, g_nr, g_npr, g_st = run_gpu_qsa(case, params_ready=params_ready, late_key_length=late_key_length,
+                                          key_length_late=key_length_late, **kw)
     assert g_st == r_st
     if past_block_keys is not None:
         # copied past rows are bit-exact copies
@@ -67,29 +68,39 @@ def stale_key_lengths(case, late):
             "mixed": torch.where(torch.arange(K.numel()) % 2 == 0, K + 3, K)}[late]
 
 
+@pytest.mark.parametrize("flag", [False, True])
 @pytest.mark.parametrize("late", ["same", "one_block_more", "ragged_less", "below_L", "huge", "mixed"])
 @pytest.mark.parametrize("L,Di,kbs,shared", [(2048, 128, 64, False), (300, 64, 32, True), (45, 256, 128, False)])
-def test_key_length_written_late_by_the_preceding_kernel(late, L, Di, kbs, shared):
+def test_key_length_written_late_by_the_preceding_kernel(late, L, Di, kbs, shared, flag):
     """The default form reads key_length before its dependency wait only as
     a prefetch hint. Here the kernel launched just before the call lets it
     start and writes key_length afterwards; the call still finds the blocks,
     carry outputs and status of the late values, whatever the stale ones
     were: the same, a block further on, a ragged amount less, shorter than L
     (no usable hint), huge (blocks beyond Bcap), or stale in every other
-    sequence only."""
+    sequence only; with and without key_length_late (no hint taken)."""
     case = wl.make_qsa_case("late", 8, L, Di=Di, Dr=64, kbs=kbs, seed=L + Di + kbs, past_max=4 * kbs + 7,
                             shared_length=shared)
-    n, _ = check(case, late_key_length=stale_key_lengths(case, late))
+    n, _ = check(case, late_key_length=stale_key_lengths(case, late), key_length_late=flag)
     assert n == case.completed_blocks()
 
 
+@pytest.mark.parametrize("flag", [False, True])
 @pytest.mark.parametrize("late", ["one_block_more", "mixed"])
-def test_key_length_written_late_full_size(late):
+def test_key_length_written_late_full_size(late, flag):
     """The benchmark's workload (32 sequences of 2048 new tokens, per-sequence
     key_length) with its key lengths written after the call has started."""
     case = wl.qsa_prepare_workload()
-    n, _ = check(case, late_key_length=stale_key_lengths(case, late))
+    n, _ = check(case, late_key_length=stale_key_lengths(case, late), key_length_late=flag)
     assert n == case.completed_blocks() == 1024
+
+
+def test_key_length_late_flag_without_a_late_write():
+    """key_length_late only drops the hint: with key_length written well
+    before the call the results are the same, full size and with carry."""
+    case = wl.qsa_prepare_workload()
+    n, _ = check(case, key_length_late=True)
+    assert n == 1024
 
 
 def test_no_block_completed_only_carry():
