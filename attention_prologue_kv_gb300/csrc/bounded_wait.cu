@@ -5,7 +5,7 @@
 // then records KVR_DEVERR_TIMEOUT and returns, leaving the context usable.
 // No copy is in flight, so the CTA may exit with the phase pending.
 //
-// Also here: a late producer of a device word, for checking that a kernel
+// Also here: a late producer of device words, for checking that a kernel
 // reads its inputs only after its dependency wait.
 #include "kvr_internal.cuh"
 
